@@ -1,0 +1,160 @@
+"""Float64 CPU oracle for the exact attention forward pass (TEST INFRASTRUCTURE).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
+this package. It is the plain definition that the CUDA library is checked
+against and shares no code with it. The arithmetic lives in ``fa_oracle.cpp``
+(C++, IEEE double, no fast-math); this module only builds and marshals.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+the pages print, closed forms, invariants and independent library routines.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.cpp into liboracle.so (portable flags: no -march, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.fa_oracle_hw_threads.restype = ctypes.c_int
+        lib.fa_oracle_attention.restype = ctypes.c_int
+        lib.fa_oracle_attention.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [
+            ctypes.c_double, ctypes.c_int, dp, dp, ctypes.c_int]
+        lib.fa_oracle_attention_rows.restype = ctypes.c_int
+        lib.fa_oracle_attention_rows.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [
+            ctypes.c_double, ctypes.c_int, i64p, ctypes.c_int64, dp, dp, ctypes.c_int]
+        lib.fa_oracle_probs.restype = None
+        lib.fa_oracle_probs.argtypes = [dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_double, ctypes.c_int, dp]
+        lib.fa_oracle_online_softmax.restype = ctypes.c_int
+        lib.fa_oracle_online_softmax.argtypes = [dp, ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
+        lib.fa_oracle_merge.restype = None
+        lib.fa_oracle_merge.argtypes = [ctypes.c_double, ctypes.c_double, dp,
+                                        ctypes.c_double, ctypes.c_double, dp, ctypes.c_int,
+                                        dp, dp, dp]
+        lib.fa_oracle_block_state.restype = None
+        lib.fa_oracle_block_state.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int64,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                              ctypes.c_int, dp, dp, dp]
+        _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def hw_threads() -> int:
+    return int(_load().fa_oracle_hw_threads())
+
+
+def attention(Q, K, V, scale: float, causal: bool, nthreads: int = 0):
+    """O [B,H,Nq,d], L [B,H,Nq] by the plain definition. Q: [B,H,Nq,d]; K, V: [B,H,Nk,d]."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    assert K.shape == (B, H, Nk, d) and V.shape == (B, H, Nk, d)
+    O = np.empty((B, H, Nq, d), np.float64)
+    L = np.empty((B, H, Nq), np.float64)
+    _load().fa_oracle_attention(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d, float(scale),
+                                int(bool(causal)), _ptr(O), _ptr(L), int(nthreads))
+    return O, L
+
+
+def attention_rows(Q, K, V, scale: float, causal: bool, rows, nthreads: int = 0):
+    """The definition on selected flat rows r = (b*H + h)*Nq + i. Returns O [n,d], L [n]."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert rows.ndim == 1 and (rows.size == 0 or (rows.min() >= 0 and rows.max() < B * H * Nq))
+    n = rows.size
+    O = np.empty((n, d), np.float64)
+    L = np.empty((n,), np.float64)
+    _load().fa_oracle_attention_rows(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d, float(scale),
+                                     int(bool(causal)),
+                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+                                     _ptr(O), _ptr(L), int(nthreads))
+    return O, L
+
+
+def probs(Q, K, scale: float, causal: bool):
+    """P [Nq, Nk] of one head. Q: [Nq,d], K: [Nk,d]."""
+    Q, K = _f64(Q), _f64(K)
+    Nq, d = Q.shape
+    Nk = K.shape[0]
+    P = np.empty((Nq, Nk), np.float64)
+    _load().fa_oracle_probs(_ptr(Q), _ptr(K), Nq, Nk, d, float(scale), int(bool(causal)), _ptr(P))
+    return P
+
+
+def online_softmax(x, block: int):
+    """(m, l, m_trace, l_trace) of the online softmax recurrence over chunks of `block`."""
+    x = _f64(x).ravel()
+    n = x.size
+    nchunks = (n + block - 1) // block
+    mt = np.empty(max(nchunks, 1), np.float64)
+    lt = np.empty(max(nchunks, 1), np.float64)
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    c = _load().fa_oracle_online_softmax(_ptr(x), n, int(block), ctypes.byref(m), ctypes.byref(l),
+                                         _ptr(mt), _ptr(lt))
+    return m.value, l.value, mt[:c].copy(), lt[:c].copy()
+
+
+def merge(a, b):
+    """Merge two states (m, d, o) -> (m, d, o); o may be None for the (m, d) pair."""
+    ma, da, oa = a
+    mb, db, ob = b
+    if oa is None:
+        oa = np.zeros(0)
+        ob = np.zeros(0)
+    oa, ob = _f64(oa).ravel(), _f64(ob).ravel()
+    assert oa.size == ob.size
+    out = np.empty(oa.size, np.float64)
+    m = ctypes.c_double()
+    d = ctypes.c_double()
+    _load().fa_oracle_merge(float(ma), float(da), _ptr(oa), float(mb), float(db), _ptr(ob),
+                            oa.size, ctypes.byref(m), ctypes.byref(d), _ptr(out))
+    return m.value, d.value, out
+
+
+def block_state(q, K, V, i: int, j0: int, j1: int, scale: float, causal: bool):
+    """The (m, d, o~) state of keys [j0, j1) for query row i (q: [d], K, V: [Nk, d])."""
+    q, K, V = _f64(q).ravel(), _f64(K), _f64(V)
+    d = q.size
+    out = np.empty(d, np.float64)
+    m = ctypes.c_double()
+    den = ctypes.c_double()
+    _load().fa_oracle_block_state(_ptr(q), _ptr(K), _ptr(V), d, int(i), int(j0), int(j1),
+                                  float(scale), int(bool(causal)), ctypes.byref(m),
+                                  ctypes.byref(den), _ptr(out))
+    return m.value, den.value, out

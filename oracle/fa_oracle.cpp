@@ -1,0 +1,236 @@
+// fa_oracle.cpp -- plain float64 CPU oracle for the exact attention forward pass.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the definition the CUDA path is checked
+// against; it is built by the test harness and is called only by the tests, by
+// the smoke check and by the benchmark's CPU-baseline leg. No product code path
+// links, loads or calls it, and it shares no code, header or constant with the
+// CUDA library.
+//
+// Everything is computed in IEEE double from inputs that the caller has already
+// widened (exactly) from fp16/bf16. Nothing is blocked, fused or reordered
+// beyond what each cited definition states.
+//
+// Sources (web pages, cited by title and section):
+//   [CS336] CS336 lecture 5 code "05_flash_attention.py":
+//           part 1 "在线 softmax" (online_softmax_stats) and
+//           part 2 "FlashAttention 前向" (standard_attention, flash_attention_forward).
+//   [CA]    "Flash Attention" (blog.cyberangel.work): sections "Online Softmax"
+//           (safe softmax, 3 passes) and "平行化" (the (m, d) and (m, d, o~) merge).
+//   [HW]    "手写 Flash Attention：从算法原理到高性能实现": section 2.2 "Online Softmax"
+//           (the worked row [2,1,5,3] with block 2).
+//
+// Pins (what fixes each function other than itself) live in tests/test_oracle_pins.py.
+// Every exported function is pinned; none is "parity unpinned".
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+#include <algorithm>
+
+namespace {
+
+const double NEG_INF = -std::numeric_limits<double>::infinity();
+
+// One output row of attention by the plain definition ([CS336] part 2,
+// standard_attention; [CA] "Why Flash Attention"):
+//   s_j = scale * <q, k_j>            for every key j (the whole row is materialised)
+//   s_j = -inf  if causal and j > i   (query i sees key j iff j <= i; top-left aligned,
+//                                      the triu(1) mask of standard_attention)
+//   p   = safe softmax of s           ([CA] "Safe softmax (3 遍掃描)": max, sum, divide)
+//   o   = sum_j p_j v_j
+//   L   = m + ln(sum_j exp(s_j - m))  (logsumexp, [CS336] part 2 "L_i = m_i + log(l_i)")
+void attention_row(const double* q, const double* K, const double* V,
+                   int Nk, int d, double scale, bool causal, int64_t i,
+                   double* s /* scratch [Nk] */, double* o /* [d] */, double* L) {
+    // scores
+    for (int j = 0; j < Nk; ++j) {
+        if (causal && (int64_t)j > i) { s[j] = NEG_INF; continue; }
+        const double* k = K + (int64_t)j * d;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += q[c] * k[c];
+        s[j] = scale * acc;
+    }
+    // pass 1: row max
+    double m = NEG_INF;
+    for (int j = 0; j < Nk; ++j) m = std::max(m, s[j]);
+    // pass 2: denominator
+    double den = 0.0;
+    for (int j = 0; j < Nk; ++j) den += std::exp(s[j] - m);
+    // pass 3: normalised probabilities, written over the scores (P row materialised)
+    for (int j = 0; j < Nk; ++j) s[j] = std::exp(s[j] - m) / den;
+    // o = P V
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int j = 0; j < Nk; ++j) {
+        const double p = s[j];
+        if (p == 0.0) continue;
+        const double* v = V + (int64_t)j * d;
+        for (int c = 0; c < d; ++c) o[c] += p * v[c];
+    }
+    *L = m + std::log(den);
+}
+
+template <class F>
+void parallel_for(int64_t n, int nthreads, F&& f) {
+    if (nthreads <= 0) nthreads = (int)std::max(1u, std::thread::hardware_concurrency());
+    if (nthreads > n) nthreads = (int)std::max<int64_t>(1, n);
+    if (nthreads == 1) { f(0, n); return; }
+    std::vector<std::thread> th;
+    th.reserve(nthreads);
+    // interleaved chunks so that causal rows (whose cost grows with i) balance
+    const int64_t chunk = 16;
+    for (int t = 0; t < nthreads; ++t) {
+        th.emplace_back([&, t]() {
+            for (int64_t c0 = (int64_t)t * chunk; c0 < n; c0 += (int64_t)nthreads * chunk)
+                f(c0, std::min(n, c0 + chunk));
+        });
+    }
+    for (auto& x : th) x.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Number of threads the oracle uses when asked for 0 (all host cores).
+int fa_oracle_hw_threads(void) {
+    return (int)std::max(1u, std::thread::hardware_concurrency());
+}
+
+// Full attention forward by the plain definition (see attention_row).
+// Q, O: [B,H,Nq,d]; K, V: [B,H,Nk,d]; L: [B,H,Nq]; all float64, row-major, dense.
+// nthreads <= 0 uses every host core. Returns the number of threads used.
+int fa_oracle_attention(const double* Q, const double* K, const double* V,
+                        int B, int H, int Nq, int Nk, int d, double scale, int causal,
+                        double* O, double* L, int nthreads) {
+    const int64_t rows = (int64_t)B * H * Nq;
+    if (nthreads <= 0) nthreads = fa_oracle_hw_threads();
+    parallel_for(rows, nthreads, [&](int64_t r0, int64_t r1) {
+        std::vector<double> s((size_t)std::max(Nk, 1));
+        for (int64_t r = r0; r < r1; ++r) {
+            const int64_t bh = r / Nq, i = r % Nq;
+            attention_row(Q + r * d, K + bh * (int64_t)Nk * d, V + bh * (int64_t)Nk * d,
+                          Nk, d, scale, causal != 0, i, s.data(), O + r * d, L + r);
+        }
+    });
+    return nthreads;
+}
+
+// The same definition evaluated only on selected rows. rows[t] is a flat row index
+// b*H*Nq + h*Nq + i; O_rows is [nrows, d], L_rows is [nrows]. Q is [B,H,Nq,d],
+// K and V are [B,H,Nk,d] (the full tensors).
+int fa_oracle_attention_rows(const double* Q, const double* K, const double* V,
+                             int B, int H, int Nq, int Nk, int d, double scale, int causal,
+                             const int64_t* rows, int64_t nrows,
+                             double* O_rows, double* L_rows, int nthreads) {
+    (void)B; (void)H;
+    if (nthreads <= 0) nthreads = fa_oracle_hw_threads();
+    parallel_for(nrows, nthreads, [&](int64_t t0, int64_t t1) {
+        std::vector<double> s((size_t)std::max(Nk, 1));
+        for (int64_t t = t0; t < t1; ++t) {
+            const int64_t r = rows[t];
+            const int64_t bh = r / Nq, i = r % Nq;
+            attention_row(Q + r * d, K + bh * (int64_t)Nk * d, V + bh * (int64_t)Nk * d,
+                          Nk, d, scale, causal != 0, i, s.data(), O_rows + t * d, L_rows + t);
+        }
+    });
+    return nthreads;
+}
+
+// The probability matrix P of one head by the same definition: P is [Nq, Nk].
+// Q is [Nq,d], K is [Nk,d]. Used by the invariant pins (rows sum to one).
+void fa_oracle_probs(const double* Q, const double* K, int Nq, int Nk, int d,
+                     double scale, int causal, double* P) {
+    std::vector<double> o((size_t)d), vdummy((size_t)Nk * d, 0.0);
+    for (int64_t i = 0; i < Nq; ++i) {
+        double Lr;
+        // attention_row leaves the normalised probabilities in its scratch row.
+        attention_row(Q + i * d, K, vdummy.data(), Nk, d, scale, causal != 0, i,
+                      P + i * (int64_t)Nk, o.data(), &Lr);
+    }
+}
+
+// Online softmax statistics ([CS336] part 1, online_softmax_stats; [CA] "Online
+// softmax (2 遍掃描)"): read x in chunks of `block`; keep m = running max and
+// l = sum exp(x - m); when a chunk raises the max to m_new, re-base the old sum:
+//   m_new = max(m, max(chunk));  l = l * exp(m - m_new) + sum_chunk exp(x - m_new).
+// The state after every chunk is written to m_trace[c], l_trace[c] when those are
+// non-null (the worked example on the [HW] page prints these intermediates).
+// Returns the number of chunks.
+int fa_oracle_online_softmax(const double* x, int n, int block,
+                             double* m_out, double* l_out,
+                             double* m_trace, double* l_trace) {
+    double m = NEG_INF, l = 0.0;
+    int c = 0;
+    for (int s = 0; s < n; s += block, ++c) {
+        const int e = std::min(n, s + block);
+        double cmax = NEG_INF;
+        for (int t = s; t < e; ++t) cmax = std::max(cmax, x[t]);
+        const double m_new = std::max(m, cmax);
+        double add = 0.0;
+        for (int t = s; t < e; ++t) add += std::exp(x[t] - m_new);
+        // exp(m - m_new) with m = -inf and a finite m_new is exp(-inf) = 0.
+        l = l * std::exp(m - m_new) + add;
+        m = m_new;
+        if (m_trace) m_trace[c] = m;
+        if (l_trace) l_trace[c] = l;
+    }
+    *m_out = m;
+    *l_out = l;
+    return c;
+}
+
+// The merge operator on partial states ([CA] "平行化"): for states (m_a, d_a, o_a) and
+// (m_b, d_b, o_b) with o of length dv (dv may be 0 for the (m, d) pair),
+//   m = max(m_a, m_b)
+//   d = d_a e^{m_a - m} + d_b e^{m_b - m}
+//   o = o_a e^{m_a - m} + o_b e^{m_b - m}
+// An empty state (m = -inf, d = 0, o = 0) is the identity: its weight e^{-inf - m} is 0.
+void fa_oracle_merge(double m_a, double d_a, const double* o_a,
+                     double m_b, double d_b, const double* o_b, int dv,
+                     double* m_out, double* d_out, double* o_out) {
+    const double m = std::max(m_a, m_b);
+    const double wa = (m_a == NEG_INF) ? 0.0 : std::exp(m_a - m);
+    const double wb = (m_b == NEG_INF) ? 0.0 : std::exp(m_b - m);
+    *m_out = m;
+    *d_out = d_a * wa + d_b * wb;
+    for (int c = 0; c < dv; ++c) o_out[c] = o_a[c] * wa + o_b[c] * wb;
+}
+
+// The state (m, d, o~) of one key block for one query row ([CA] "平行化": the
+// per-element state (x_k, 1, v_k) merged over the block): s_j = scale*<q,k_j>
+// (masked to -inf when causal and j > i), m = max_j s_j, d = sum_j e^{s_j - m},
+// o~ = sum_j e^{s_j - m} v_j. Keys j in [j0, j1). A block with every key masked
+// returns the identity state (-inf, 0, 0).
+void fa_oracle_block_state(const double* q, const double* K, const double* V, int d,
+                           int64_t i, int j0, int j1, double scale, int causal,
+                           double* m_out, double* d_out, double* o_out) {
+    std::vector<double> s((size_t)std::max(j1 - j0, 1));
+    double m = NEG_INF;
+    for (int j = j0; j < j1; ++j) {
+        double v;
+        if (causal && (int64_t)j > i) v = NEG_INF;
+        else {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += q[c] * K[(int64_t)j * d + c];
+            v = scale * acc;
+        }
+        s[(size_t)(j - j0)] = v;
+        m = std::max(m, v);
+    }
+    for (int c = 0; c < d; ++c) o_out[c] = 0.0;
+    double den = 0.0;
+    if (m != NEG_INF) {
+        for (int j = j0; j < j1; ++j) {
+            const double w = std::exp(s[(size_t)(j - j0)] - m);
+            den += w;
+            for (int c = 0; c < d; ++c) o_out[c] += w * V[(int64_t)j * d + c];
+        }
+    }
+    *m_out = m;
+    *d_out = den;
+}
+
+}  // extern "C"
