@@ -1,0 +1,126 @@
+"""Exact fused attention forward on GB300 (sm_103a): a thin ctypes binding over libfa.so.
+
+The binding only marshals arguments: every step of the computation runs in the CUDA
+kernels of ``libfa.so`` (source in ``csrc/``, C ABI in ``include/fa_fwd.h``). There is
+no CPU or PyTorch fallback: importing this package fails loudly when the library has
+not been built (``python -c "import __graft_entry__ as g; g.build()"``).
+
+Function names follow the C ABI:
+    fa_fwd(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream) -> status
+plus a tensor-level convenience ``attention(q, k, v, causal, scale)`` -> (O, L).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_F16 = 0
+FA_BF16 = 1
+
+STATUS = {
+    0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_HEAD_DIM", -3: "FA_ERR_SHAPE",
+    -4: "FA_ERR_EMPTY_KEYS", -5: "FA_ERR_SCALE", -6: "FA_ERR_ALIGN", -7: "FA_ERR_DTYPE",
+    -8: "FA_ERR_CUDA", -9: "FA_ERR_TENSOR_MAP", -10: "FA_ERR_DEVICE", -11: "FA_ERR_TIMEOUT",
+}
+globals().update({v: k for k, v in STATUS.items()})
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, what: str = "fa_fwd"):
+        self.code = code
+        super().__init__(f"{what} failed: {STATUS.get(code, code)} ({strerror(code)})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libfa.so is not built ({LIB_PATH} missing); run __graft_entry__.build() first. "
+            "There is no fallback implementation.")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp = ctypes.c_void_p
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_last_status.restype = ctypes.c_int
+    lib.fa_last_status.argtypes = []
+    lib.fa_clear_status.restype = ctypes.c_int
+    lib.fa_clear_status.argtypes = []
+    lib.fa_strerror.restype = ctypes.c_char_p
+    lib.fa_strerror.argtypes = [ctypes.c_int]
+    lib.fa_selftest_wait_timeout.restype = ctypes.c_int
+    lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
+    lib.fa_num_kernel_launches.restype = ctypes.c_longlong
+    lib.fa_num_kernel_launches.argtypes = []
+    return lib
+
+
+lib = _load()
+
+
+def strerror(code: int) -> str:
+    return lib.fa_strerror(int(code)).decode()
+
+
+def fa_fwd(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream) -> int:
+    """Direct C-ABI call with raw integer addresses (device pointers) and sizes."""
+    return int(lib.fa_fwd(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
+                          float(scale), int(bool(causal)), int(dtype), stream))
+
+
+def fa_last_status() -> int:
+    return int(lib.fa_last_status())
+
+
+def fa_clear_status() -> int:
+    return int(lib.fa_clear_status())
+
+
+def fa_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    return int(lib.fa_selftest_wait_timeout(int(limit_us), stream))
+
+
+def fa_num_kernel_launches() -> int:
+    return int(lib.fa_num_kernel_launches())
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+              stream=None):
+    """O, L = attention(q, k, v) for CUDA tensors q [B,H,Nq,d], k/v [B,H,Nk,d] (fp16/bf16).
+
+    Allocates O (like q) and L ([B,H,Nq] fp32) unless given; launches on `stream`
+    (a torch.cuda.Stream, default: the current stream) and returns without synchronising.
+    """
+    import torch
+
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("q, k, v must be float16 or bfloat16")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H, d")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_F16
+    with torch.cuda.device(q.device):
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, Nq, Nk, d, scale, causal, dt, ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise FAError(rc)
+    return out, lse

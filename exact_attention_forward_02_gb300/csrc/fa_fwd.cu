@@ -1,0 +1,740 @@
+// fa_fwd.cu -- exact fused attention forward for GB300 (sm_103a) and its C ABI.
+//
+// What it computes (CS336 lecture 5 "05_flash_attention.py", part 2, flash_attention_forward;
+// "Flash Attention" (blog.cyberangel.work), sections "Online Softmax" and "平行化"):
+// for each query tile Q_i and each key/value tile (K_j, V_j), in order of j,
+//     S    = tau * Q_i K_j^T            (masked to -inf where a key is not visible)
+//     m'   = max(m, rowmax(S))
+//     P    = exp(S - m')
+//     l    = exp(m - m') l + rowsum(P)
+//     O~   = exp(m - m') O~ + P V_j
+// and finally O = O~ / l, L = m + ln l. The scores never leave the SM.
+//
+// GB300 mapping (one persistent CTA per SM, 10 warps):
+//   warp 8      TMA producer: loads the two 128-row Q tiles of a work item once, then
+//               streams K_j, V_j through a ring of shared-memory slots (mbarrier pipeline).
+//   warp 9      MMA issuer: one thread issues tcgen05.mma for S = Q K^T (both operands
+//               K-major in shared memory, fp32 accumulator in Tensor Memory) and for
+//               O~ += P V (P from shared memory or Tensor Memory, V MN-major in shared
+//               memory), and signals completion with tcgen05.commit.
+//   warps 0-7   two softmax warpgroups, one per Q tile (ping-pong): thread r owns query
+//               row r of its tile (TMEM lane r), reads its 128 scores with tcgen05.ld,
+//               applies the mask, keeps (m, l) in registers in base-2 units (the scale is
+//               folded with log2(e)), writes P as 16-bit values, rescales O~ in TMEM when
+//               the running max grows by more than 2^8, and runs the epilogue.
+// Work items are (batch*head, 256-row query block); causal items run heaviest first.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "fa_fwd.h"
+#include "sm103_ptx.cuh"
+
+#ifndef FA_P_IN_TMEM
+#define FA_P_IN_TMEM 1
+#endif
+
+// Device-side status word (one per device that loads the library).
+__device__ int g_fa_status;
+
+namespace fa {
+
+constexpr int BM = 128;                  // query rows per tile = TMEM lanes
+constexpr int BN = 128;                  // keys per K/V tile
+constexpr int NUM_WARPS = 10;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int WARP_LOAD = 8;
+constexpr int WARP_MMA = 9;
+constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O0 | O1, 128 columns each
+constexpr uint32_t TMEM_S0 = 0, TMEM_O0 = 256;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O~ only when m grows > 2^8
+constexpr int SMEM_LIMIT = 232448;       // 227 KB opt-in dynamic shared memory per CTA
+constexpr int MAX_SLOTS = 8;
+
+struct Barriers {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[MAX_SLOTS], kv_empty[MAX_SLOTS];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, bool P_TMEM>
+struct Layout {
+  static constexpr int TILE_BYTES = BM * D * 2;       // one Q, K or V tile
+  static constexpr int CHUNK_BYTES = BM * 128;        // 128 rows x one 128-byte swizzle span
+  static constexpr int CHUNKS = D / 64;               // 64 16-bit elements per span
+  static constexpr int P_BYTES = P_TMEM ? 0 : BM * BN * 2;
+  static constexpr int FIXED = 2 * TILE_BYTES + 2 * P_BYTES + 1024 /*align*/ + 512 /*bars*/;
+  static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TILE_BYTES;
+  static constexpr int KV_SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_P = OFF_KV + KV_SLOTS * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(Barriers) + 1024;
+  static_assert(KV_SLOTS >= 2, "need at least two K/V slots");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+};
+
+struct Params {
+  void* O;
+  float* L;
+  int BH, Nq, Nk;
+  int n_qblk;      // ceil(Nq / 256)
+  int n_items;     // n_qblk * BH
+  int n_kv_all;    // ceil(Nk / 128)
+  float c;         // scale * log2(e)
+  unsigned long long wait_limit_ns;
+};
+
+// ----------------------------------------------------------------------------- waits
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicCAS(&g_fa_status, 0, FA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+// Drain wait used on the way out after an abort: ignores the abort flag, still bounded.
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicCAS(&g_fa_status, 0, FA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bounded wait: true when the phase of `parity` completed; false when the wait gave up
+// (the status word then holds FA_ERR_TIMEOUT) or another role already gave up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, limit_ns);
+}
+
+struct Item {
+  int bh, q0, n_kv;
+  bool has1;  // the second 128-row tile holds at least one valid query row
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Item decode_item(int t, const Params& p) {
+  Item it;
+  int qblk;
+  if (CAUSAL) {  // heaviest (last) query blocks first
+    qblk = p.n_qblk - 1 - t / p.BH;
+    it.bh = t % p.BH;
+  } else {       // consecutive items share a head's K/V in L2
+    it.bh = t / p.n_qblk;
+    qblk = t % p.n_qblk;
+  }
+  it.q0 = qblk * 2 * BM;
+  it.has1 = it.q0 + BM < p.Nq;
+  if (CAUSAL) {
+    const int last_row = min(it.q0 + 2 * BM, p.Nq) - 1;
+    it.n_kv = min(p.n_kv_all, last_row / BN + 1);
+  } else {
+    it.n_kv = p.n_kv_all;
+  }
+  return it;
+}
+
+// ----------------------------------------------------------------------------- kernel
+template <int D, bool BF16, bool CAUSAL, bool P_TMEM>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using LY = Layout<D, P_TMEM>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + LY::OFF_BAR);
+  const uint32_t sQ = smem_u32(smem + LY::OFF_Q);
+  const uint32_t sKV = smem_u32(smem + LY::OFF_KV);
+  const uint32_t sP = smem_u32(smem + LY::OFF_P);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->q_full), 1);
+    mbar_init(smem_u32(&bars->q_empty), 1);
+    for (int s = 0; s < LY::KV_SLOTS; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(smem_u32(&bars->s_full[g]), 1);
+      mbar_init(smem_u32(&bars->p_full[g]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&bars->o_done[g]), 1);
+    }
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_LOAD && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const unsigned long long lim = p.wait_limit_ns;
+
+  if (warp == WARP_LOAD) {
+    // ======================================================================= producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      uint32_t slot = 0, ph = 0, q_ph = 0;
+      uint32_t issued_mask = 0, last_par = 0;  // for draining on abort
+      bool q_issued = false;
+      bool ok = true;
+      auto load_kv = [&](const CUtensorMap* tm, int bh, int row0) -> bool {
+        const uint32_t full = smem_u32(&bars->kv_full[slot]);
+        if (!wait_bar(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) return false;
+        mbar_arrive_expect_tx(full, LY::TILE_BYTES);
+        const uint32_t dst = sKV + slot * LY::TILE_BYTES;
+#pragma unroll
+        for (int c = 0; c < LY::CHUNKS; ++c)
+          tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, tm, full, c * 64, row0, bh, pol_kv);
+        issued_mask |= 1u << slot;
+        last_par = (last_par & ~(1u << slot)) | (ph << slot);
+        if (++slot == LY::KV_SLOTS) { slot = 0; ph ^= 1; }
+        return true;
+      };
+      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+        const Item it = decode_item<CAUSAL>(t, p);
+        ok = load_kv(&tmK, it.bh, 0);
+        if (!ok) break;
+        ok = wait_bar(smem_u32(&bars->q_empty), q_ph ^ 1, abort_flag, lim);
+        if (!ok) break;
+        q_ph ^= 1;
+        const uint32_t qf = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qf, (it.has1 ? 2 : 1) * LY::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < LY::CHUNKS; ++c)
+          tma_load_3d_hint(sQ + c * LY::CHUNK_BYTES, &tmQ, qf, c * 64, it.q0, it.bh, pol_q);
+        if (it.has1) {
+#pragma unroll
+          for (int c = 0; c < LY::CHUNKS; ++c)
+            tma_load_3d_hint(sQ + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmQ, qf, c * 64,
+                             it.q0 + BM, it.bh, pol_q);
+        }
+        q_issued = true;
+        ok = load_kv(&tmV, it.bh, 0);
+        for (int j = 1; j < it.n_kv && ok; ++j) {
+          ok = load_kv(&tmK, it.bh, j * BN);
+          if (ok) ok = load_kv(&tmV, it.bh, j * BN);
+        }
+      }
+      if (!ok) {
+        // drain: every issued copy must land before the CTA may exit
+        for (int s = 0; s < LY::KV_SLOTS; ++s)
+          if (issued_mask & (1u << s))
+            wait_drain(smem_u32(&bars->kv_full[s]), (last_par >> s) & 1u, lim);
+        if (q_issued) wait_drain(smem_u32(&bars->q_full), q_ph ^ 1, lim);
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ======================================================================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BM, BN);
+      constexpr uint32_t ID_O = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BM, D);
+      uint32_t slot = 0, ph = 0, q_ph = 0;
+      uint32_t p_ph[2] = {0, 0};
+      bool ok = true;
+      auto take = [&](uint32_t& s_out, uint32_t& ph_out) {
+        s_out = slot;
+        ph_out = ph;
+        if (++slot == LY::KV_SLOTS) { slot = 0; ph ^= 1; }
+      };
+      // S_g = Q_g K^T : M=128 rows, N=128 keys, K=D (16 per instruction)
+      auto issue_s = [&](int g, uint32_t kslot) {
+        const uint32_t qa = sQ + g * LY::TILE_BYTES;
+        const uint32_t ka = sKV + kslot * LY::TILE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32;
+          umma_ss(tmem + TMEM_S0 + g * 128, umma_smem_desc(qa + off, 16, 1024),
+                  umma_smem_desc(ka + off, 16, 1024), ID_S, ks > 0 ? 1u : 0u);
+        }
+      };
+      // O_g += P_g V : M=128 rows, N=D, K=128 keys
+      auto issue_pv = [&](int g, uint32_t vslot, bool acc) {
+        const uint32_t va = sKV + vslot * LY::TILE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t bdesc = umma_smem_desc(va + ks * 16 * 128, LY::CHUNK_BYTES, 1024);
+          const uint32_t accf = (acc || ks > 0) ? 1u : 0u;
+          if constexpr (P_TMEM) {
+            umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8, bdesc, ID_O, accf);
+          } else {
+            const uint32_t pa = sP + g * LY::P_BYTES + (ks >> 2) * (BM * 128) + (ks & 3) * 32;
+            umma_ss(tmem + TMEM_O0 + g * 128, umma_smem_desc(pa, 16, 1024), bdesc, ID_O, accf);
+          }
+        }
+      };
+      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+        const Item it = decode_item<CAUSAL>(t, p);
+        uint32_t sK, phK;
+        take(sK, phK);
+        ok = wait_bar(smem_u32(&bars->kv_full[sK]), phK, abort_flag, lim) &&
+             wait_bar(smem_u32(&bars->q_full), q_ph, abort_flag, lim);
+        if (!ok) break;
+        q_ph ^= 1;
+        tc_fence_after();
+        issue_s(0, sK);
+        umma_commit(smem_u32(&bars->s_full[0]));
+        if (it.has1) {
+          issue_s(1, sK);
+          umma_commit(smem_u32(&bars->s_full[1]));
+        }
+        umma_commit(smem_u32(&bars->kv_empty[sK]));
+        for (int j = 0; j < it.n_kv; ++j) {
+          uint32_t sV, phV, sKn = 0, phKn = 0;
+          take(sV, phV);
+          const bool has_next = j + 1 < it.n_kv;
+          if (has_next) take(sKn, phKn);
+          ok = wait_bar(smem_u32(&bars->kv_full[sV]), phV, abort_flag, lim) &&
+               wait_bar(smem_u32(&bars->p_full[0]), p_ph[0], abort_flag, lim);
+          if (!ok) break;
+          p_ph[0] ^= 1;
+          tc_fence_after();
+          issue_pv(0, sV, j > 0);
+          umma_commit(smem_u32(&bars->o_done[0]));
+          if (!it.has1) umma_commit(smem_u32(&bars->kv_empty[sV]));
+          if (has_next) {
+            ok = wait_bar(smem_u32(&bars->kv_full[sKn]), phKn, abort_flag, lim);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(0, sKn);
+            umma_commit(smem_u32(&bars->s_full[0]));
+          }
+          if (it.has1) {
+            ok = wait_bar(smem_u32(&bars->p_full[1]), p_ph[1], abort_flag, lim);
+            if (!ok) break;
+            p_ph[1] ^= 1;
+            tc_fence_after();
+            issue_pv(1, sV, j > 0);
+            umma_commit(smem_u32(&bars->o_done[1]));
+            umma_commit(smem_u32(&bars->kv_empty[sV]));
+            if (has_next) {
+              issue_s(1, sKn);
+              umma_commit(smem_u32(&bars->s_full[1]));
+            }
+          }
+          if (has_next) umma_commit(smem_u32(&bars->kv_empty[sKn]));
+        }
+        if (ok) umma_commit(smem_u32(&bars->q_empty));
+      }
+      // make sure every issued MMA has finished before TMEM can be released
+      umma_commit(smem_u32(&bars->mma_drain));
+      wait_drain(smem_u32(&bars->mma_drain), 0, lim);
+    }
+  } else {
+    // ======================================================================= softmax
+    const int g = warp >> 2;         // which Q tile / warpgroup
+    const int wq = warp & 3;         // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;    // row within the tile
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + TMEM_S0 + g * 128;
+    const uint32_t tO = tmem + lane_off + TMEM_O0 + g * 128;
+    const float c = p.c;
+    uint32_t s_ph = 0, o_ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      const Item it = decode_item<CAUSAL>(t, p);
+      if (g == 1 && !it.has1) continue;
+      const int row = it.q0 + g * BM + r;
+      const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, kv_lim) visible
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        bool w = wait_bar(smem_u32(&bars->s_full[g]), s_ph, abort_flag, lim);
+        if (j > 0 && w) w = wait_bar(smem_u32(&bars->o_done[g]), o_ph, abort_flag, lim);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        s_ph ^= 1;
+        if (j > 0) o_ph ^= 1;
+        tc_fence_after();
+
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+        tmem_wait_ld();
+
+        const int vis = kv_lim - j * BN;
+        const bool full = vis >= BN;
+        // raw row max over visible keys
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            mx[k & 7] = fmaxf(mx[k & 7], k < vis ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY);
+        }
+        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_tile = (mt == -INFINITY) ? -INFINITY : mt * c;
+        float m_new = m_run, alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_new = m_tile;
+        } else if (m_tile > m_run + RESCALE_THRESHOLD) {
+          m_new = m_tile;
+          alpha = ex2_approx(m_run - m_new);
+          rescale = true;
+        }
+        const float nb = (m_new == -INFINITY) ? 0.f : -m_new;
+        float sum[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+        // P = exp2(S*c - m) in fp32 for the row sum, packed to 16-bit pairs (key 2k in
+        // the low half, key 2k+1 in the high half) for the second product
+        uint32_t pk[2][32];
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[(2 * k) >> 5][(2 * k) & 31]), c, nb));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[(2 * k + 1) >> 5][(2 * k + 1) & 31]), c, nb));
+            sum[(2 * k) & 7] += p0;
+            sum[(2 * k + 1) & 7] += p1;
+            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const float p0 = (2 * k < vis)
+                ? ex2_approx(fmaf(__uint_as_float(sr[(2 * k) >> 5][(2 * k) & 31]), c, nb)) : 0.f;
+            const float p1 = (2 * k + 1 < vis)
+                ? ex2_approx(fmaf(__uint_as_float(sr[(2 * k + 1) >> 5][(2 * k + 1) & 31]), c, nb)) : 0.f;
+            sum[(2 * k) & 7] += p0;
+            sum[(2 * k + 1) & 7] += p1;
+            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+          }
+        }
+        const float ls = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+
+        // rescale O~ (in TMEM) when this row's max grew past the threshold
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(tO + q * 32, o);
+          }
+        }
+        l_run = l_run * alpha + ls;
+        m_run = m_new;
+
+        if constexpr (P_TMEM) {
+          // P overwrites the first 64 columns of this tile's S region
+          tmem_st32(tS, pk[0]);
+          tmem_st32(tS + 32, pk[1]);
+          tmem_wait_st();
+        } else {
+          tmem_wait_st();
+          // K-major tile with the 128-byte swizzle: row r at r*128 within each 64-key
+          // span, 16-byte unit u stored at unit (u ^ (r mod 8))
+          const uint32_t prow = sP + g * LY::P_BYTES + r * 128;
+          const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t addr = prow + cc * (BM * 128) + ((u ^ sw) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[cc][u * 4]),
+                           "r"(pk[cc][u * 4 + 1]), "r"(pk[cc][u * 4 + 2]), "r"(pk[cc][u * 4 + 3])
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[g]));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------------ epilogue
+      {
+        const bool w = wait_bar(smem_u32(&bars->o_done[g]), o_ph, abort_flag, lim);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        o_ph ^= 1;
+        tc_fence_after();
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        const bool valid = row < p.Nq;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
+                        ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + q * 32, o);
+          tmem_wait_ld();
+          uint32_t w16[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+          }
+        }
+        if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+        tc_fence_before();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Bounded-wait self test: one barrier that nothing ever signals.
+__global__ void fa_wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)wait_bar(smem_u32(&bar), 0, &abort_flag, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace fa
+
+// ============================================================================= host side
+namespace {
+
+using namespace fa;
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait
+std::atomic<long long> g_launches{0};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [BH, N, d] 16-bit tensor; boxes of 64 elements (128 bytes) x 128 rows x 1 head,
+// 128-byte swizzle; rows past N read as zeros (never the next head's rows).
+int make_map(CUtensorMap* m, const void* base, int d, int N, int BH, bool bf16) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return FA_ERR_TENSOR_MAP;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_TENSOR_MAP;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+  bool attr_set[2][2][2] = {};
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FA_ERR_DEVICE;
+    di.sms = sms;
+    di.ok = true;
+  }
+  *out = &di;
+  return FA_OK;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
+           DeviceInfo* di, cudaStream_t st) {
+  constexpr bool PT = FA_P_IN_TMEM != 0;
+  using LY = Layout<D, PT>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, PT>;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    bool& set = di->attr_set[D == 128][BF16][CAUSAL];
+    if (!set) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
+      set = true;
+    }
+  }
+  const int grid = p.n_items < di->sms ? p.n_items : di->sms;
+  kern<<<grid, NUM_THREADS, LY::SMEM_BYTES, st>>>(mq, mk, mv, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq,
+           int Nk, int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  // ---- host-side argument checks (no CUDA call before they pass)
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (!(scale >= 0.f) || !isfinite(scale)) return FA_ERR_SCALE;
+  const long long BH = (long long)B * H;
+  if (BH == 0 || Nq == 0) return FA_OK;  // nothing to compute
+  if (Nk == 0) return FA_ERR_EMPTY_KEYS;
+  if (BH > 0x7fffffffLL) return FA_ERR_SHAPE;
+  const long long n_qblk = ((long long)Nq + 2 * BM - 1) / (2 * BM);
+  if (n_qblk * BH > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (!Q || !K || !V || !O || !L) return FA_ERR_NULL;
+  if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)O) & 15) return FA_ERR_ALIGN;
+  if ((uintptr_t)L & 3) return FA_ERR_ALIGN;
+
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc != FA_OK) return rc;
+
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, Q, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mk, K, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mv, V, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+
+  Params p;
+  p.O = O;
+  p.L = L;
+  p.BH = (int)BH;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qblk = (int)n_qblk;
+  p.n_items = (int)(n_qblk * BH);
+  p.n_kv_all = (Nk + BN - 1) / BN;
+  p.c = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch<64, false, false>(mq, mk, mv, p, di, st);
+    case 1: return launch<64, false, true>(mq, mk, mv, p, di, st);
+    case 2: return launch<64, true, false>(mq, mk, mv, p, di, st);
+    case 3: return launch<64, true, true>(mq, mk, mv, p, di, st);
+    case 4: return launch<128, false, false>(mq, mk, mv, p, di, st);
+    case 5: return launch<128, false, true>(mq, mk, mv, p, di, st);
+    case 6: return launch<128, true, false>(mq, mk, mv, p, di, st);
+    default: return launch<128, true, true>(mq, mk, mv, p, di, st);
+  }
+}
+
+int fa_last_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return v;
+}
+
+int fa_clear_status(void) {
+  const int z = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  return cudaMemcpyToSymbol(g_fa_status, &z, sizeof(int)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_HEAD_DIM: return "head dimension d must be 64 or 128";
+    case FA_ERR_SHAPE: return "B, H, Nq or Nk out of range";
+    case FA_ERR_EMPTY_KEYS: return "Nk is 0 but there are query rows (softmax of an empty row)";
+    case FA_ERR_SCALE: return "scale must be finite and >= 0";
+    case FA_ERR_ALIGN: return "Q, K, V, O must be 16-byte aligned and L 4-byte aligned";
+    case FA_ERR_DTYPE: return "dtype must be FA_F16 or FA_BF16";
+    case FA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case FA_ERR_TENSOR_MAP: return "the driver rejected a TMA tensor map";
+    case FA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case FA_ERR_TIMEOUT: return "a device-side pipeline wait exceeded its time limit";
+    default: return "unknown status code";
+  }
+}
+
+int fa_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA_ERR_SHAPE;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc != FA_OK) return rc;
+  fa::fa_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      (unsigned long long)limit_us * 1000ull);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+long long fa_num_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+/* fa_fwd.h -- C ABI of libfa: exact fused attention forward on one GB300 (sm_103a).
+ *
+ * The operation (per batch b, head h, query row i):
+ *     s_ij = scale * <Q[b,h,i,:], K[b,h,j,:]>            for key j in [0, Nk)
+ *     s_ij = -inf  if causal and j > i                  (top-left aligned mask)
+ *     O[b,h,i,:] = sum_j softmax_j(s_i.) V[b,h,j,:]
+ *     L[b,h,i]   = ln sum_j exp(s_ij)                   (natural-log logsumexp)
+ * as defined on the CS336 lecture 5 page "05_flash_attention.py", part 2
+ * ("FlashAttention 前向": standard_attention and flash_attention_forward, which
+ * returns (O, L) with L = m + log(l)), with the scale tau of Algorithm 2 on the
+ * "Flash Attention" page (blog.cyberangel.work). The kernel evaluates it tile by
+ * tile with the online-softmax statistics (m, l) and an unnormalised output
+ * accumulator; the Nq x Nk scores and probabilities never reach global memory.
+ *
+ * Precision: Q, K, V, O are fp16 or bf16; products are accumulated in fp32; the
+ * probabilities fed to the second product are rounded to the input type; L is fp32.
+ */
+#ifndef FA_FWD_H
+#define FA_FWD_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of Q, K, V and O. */
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* Status codes. 0 = success; every error is negative. */
+enum {
+  FA_OK = 0,
+  FA_ERR_NULL = -1,        /* a required pointer is NULL                                  */
+  FA_ERR_HEAD_DIM = -2,    /* d is not 64 or 128                                          */
+  FA_ERR_SHAPE = -3,       /* B, H, Nq or Nk negative, or B*H*N too large                  */
+  FA_ERR_EMPTY_KEYS = -4,  /* Nk == 0 while there are query rows: softmax of an empty row */
+  FA_ERR_SCALE = -5,       /* scale is negative, NaN or infinite                          */
+  FA_ERR_ALIGN = -6,       /* Q, K, V or O not 16-byte aligned, or L not 4-byte aligned   */
+  FA_ERR_DTYPE = -7,       /* dtype is not FA_F16 or FA_BF16                              */
+  FA_ERR_CUDA = -8,        /* a CUDA runtime call or the kernel launch failed             */
+  FA_ERR_TENSOR_MAP = -9,  /* the driver rejected a TMA tensor map for these arguments    */
+  FA_ERR_DEVICE = -10,     /* the current device is not an sm_103 GPU                     */
+  FA_ERR_TIMEOUT = -11     /* device-side: a pipeline wait exceeded its time limit        */
+};
+
+/* fa_fwd -- launch the attention forward pass on `stream`.
+ *
+ * Arguments (all pointers are DEVICE pointers owned by the caller):
+ *   Q      [B, H, Nq, d]  dense row-major, element type `dtype`, 16-byte aligned
+ *   K, V   [B, H, Nk, d]  dense row-major, element type `dtype`, 16-byte aligned
+ *   O      [B, H, Nq, d]  output, dense row-major, `dtype`, 16-byte aligned
+ *   L      [B, H, Nq]     output, fp32, natural-log logsumexp of each score row
+ *   d      head dimension, 64 or 128
+ *   scale  multiplies Q K^T before the softmax (1/sqrt(d) in the usual use); >= 0
+ *   causal non-zero: query i sees key j iff j <= i (top-left aligned when Nq != Nk,
+ *          so every query row sees at least key 0)
+ *   stream a cudaStream_t (NULL = the legacy default stream)
+ *
+ * Layout: no padding; row i of head (b, h) of Q starts at element ((b*H + h)*Nq + i)*d.
+ * Ownership: the library allocates no device memory and keeps no pointer after return.
+ * Timing: asynchronous. Returns FA_OK once the launch is queued; O and L are valid
+ *   after `stream` is synchronised. Calls on different streams that write the same
+ *   O/L race.
+ * Errors: argument checks happen on the host before any CUDA call and return the
+ *   FA_ERR_* code without touching the device. B == 0, H == 0 or Nq == 0 is a no-op
+ *   that returns FA_OK (pointers are not inspected). A failed CUDA call returns
+ *   FA_ERR_CUDA (the CUDA error is then readable with cudaGetLastError). Device-side
+ *   failures (a wait timeout) are reported by fa_last_status().
+ */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
+           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           fa_dtype dtype, void* stream);
+
+/* fa_last_status -- synchronise the current device, then return the device-side status
+ * word of libfa on that device: FA_OK, or the first error a kernel recorded since the
+ * last fa_clear_status() (FA_ERR_TIMEOUT when a bounded pipeline wait gave up; the kernel
+ * then returns without finishing and O/L are undefined). Returns FA_ERR_CUDA if the
+ * synchronisation itself fails. */
+int fa_last_status(void);
+
+/* fa_clear_status -- reset the device-side status word of the current device to FA_OK.
+ * Returns FA_OK or FA_ERR_CUDA. */
+int fa_clear_status(void);
+
+/* fa_strerror -- static, human-readable text for a status code (never NULL). */
+const char* fa_strerror(int code);
+
+/* fa_selftest_wait_timeout -- exercise the bounded-wait failure path without any fault:
+ * launches one CTA on `stream` that waits on a pipeline barrier nothing ever signals,
+ * with a wait limit of `limit_us` microseconds (1..1000000). The wait gives up, records
+ * FA_ERR_TIMEOUT in the status word and the kernel returns normally; the context stays
+ * usable. Returns FA_OK once queued, FA_ERR_SHAPE for a limit out of range, FA_ERR_DEVICE
+ * or FA_ERR_CUDA on failure to launch. */
+int fa_selftest_wait_timeout(int limit_us, void* stream);
+
+/* fa_num_kernel_launches -- number of kernels libfa has launched in this process
+ * (all devices), for accounting launches in a timed region. */
+long long fa_num_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_FWD_H */

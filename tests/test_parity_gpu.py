@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle, element by
+element, on the same seeded inputs.
+
+Small and medium cases are compared on every output element; the full-size workloads
+(in the launch configuration the benchmark times) are compared on sampled rows that the
+oracle computes one by one, plus properties that hold at any size.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+from tests.fa_testlib import TOL_L, TOL_O, compare, oracle_rows, run_cuda, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_forward_02_gb300 as fa
+    fa.fa_clear_status()
+    return fa
+
+
+def _full_case(w, v_std=None):
+    """Whole-output comparison. v_std: draw V with this std instead of w.std (a sharp
+    softmax from large Q and K, with values of unit size so that the absolute tolerance
+    keeps its meaning)."""
+    import oracle
+    q, k, v = gen.make_qkv(w)
+    if v_std is not None:
+        v = gen.make_qkv(gen.custom(w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, w.causal, v_std, w.seed))[2]
+    O, L = run_cuda(w, q, k, v)
+    Oref, Lref = oracle.attention(gen.to_f64_numpy(q), gen.to_f64_numpy(k), gen.to_f64_numpy(v),
+                                  w.scale, w.causal)
+    return compare(w, O, L, Oref, Lref)
+
+
+# (B, H, Nq, Nk, d, dtype, causal, std of Q and K; V has std 1)
+SMALL = [
+    (1, 1, 128, 128, 64, gen.F16, False, 1.0),
+    (1, 1, 128, 128, 64, gen.F16, True, 1.0),
+    (1, 1, 1, 1, 64, gen.BF16, False, 1.0),
+    (1, 1, 1, 1, 128, gen.F16, True, 1.0),
+    (1, 2, 2, 2, 64, gen.BF16, True, 1.0),
+    (2, 1, 127, 127, 128, gen.BF16, False, 1.0),
+    (1, 2, 129, 129, 128, gen.BF16, True, 1.0),
+    (1, 1, 255, 255, 64, gen.F16, True, 1.0),
+    (1, 1, 256, 256, 128, gen.F16, False, 1.0),
+    (1, 1, 257, 257, 64, gen.BF16, True, 1.0),
+    (1, 3, 383, 383, 128, gen.BF16, True, 1.0),
+    (2, 3, 1000, 1000, 128, gen.BF16, True, 1.0),
+    (2, 3, 1000, 1000, 64, gen.F16, False, 1.0),
+    (1, 2, 1000, 4097, 64, gen.F16, False, 1.0),     # cross attention, ragged key tail
+    (1, 2, 1000, 4097, 128, gen.BF16, True, 1.0),    # causal, Nq < Nk (top-left)
+    (1, 2, 700, 130, 64, gen.F16, True, 1.0),        # causal, Nq > Nk
+    (1, 1, 3, 300, 128, gen.F16, False, 1.0),
+    (1, 1, 300, 3, 64, gen.BF16, False, 1.0),
+    (1, 2, 512, 512, 128, gen.BF16, True, 3.0),      # sharp softmax: running max moves a lot
+    (1, 2, 512, 512, 64, gen.F16, False, 3.0),
+    (4, 16, 1024, 1024, 64, gen.F16, True, 1.0),     # 256 work items: several per CTA
+    (2, 40, 512, 640, 128, gen.BF16, False, 1.0),    # 160 work items: > one per SM
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "B{}H{}_q{}k{}_d{}_{}_{}_s{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], "causal" if c[6] else "full", c[7]))
+def test_small_full_compare(case):
+    B, H, Nq, Nk, d, dt, causal, std = case
+    w = gen.custom(B, H, Nq, Nk, d, dt, causal, std, seed=1000 + sum(case[:5]))
+    r = _full_case(w, v_std=1.0)
+    print(w.describe(), r)
+    assert r["raw_ok"], r
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross"])
+def test_workload_full_compare(name):
+    w = gen.WORKLOADS[name]
+    r = _full_case(w)
+    print(name, r)
+    assert r["raw_ok"], r
+
+
+@pytest.mark.parametrize("name", ["b2h8_n4096_d128_full", "b2h8_n8192_d128_causal",
+                                  "b1h16_n32768_d128_causal_x2", "b4h12_q1000_k4097_d64_cross"])
+def test_workload_sampled_rows(name):
+    """Full-size workloads, launched exactly as the benchmark launches them, checked on
+    sampled rows (head boundaries, tile edges, random rows) against the oracle."""
+    w = gen.WORKLOADS[name]
+    q, k, v = gen.make_qkv(w)
+    O, L = run_cuda(w, q, k, v)
+    rows = sample_rows(w)
+    Oref, Lref = oracle_rows(w, q, k, v, rows)
+    r = compare(w, O, L, Oref, Lref, rows=rows)
+    print(name, r)
+    assert r["graded_ok"], r
+    if name != "b1h16_n32768_d128_causal_x2":
+        assert r["raw_ok"], r
+    # every row written and finite (NaN canary fill before the call)
+    assert torch.isfinite(O).all() and torch.isfinite(L).all()
+    if w.causal:
+        # row 0 of every head sees only key 0: O = V[0] up to one rounding, L = scale*q0.k0
+        o0 = O[:, :, 0].double()
+        v0 = v[:, :, 0].double()
+        assert (o0 - v0).abs().max().item() <= 2 * TOL_O[w.dtype] / 10 + 1e-3 * v0.abs().max().item()
+        l0 = w.scale * (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1)
+        assert (L[:, :, 0].double() - l0).abs().max().item() <= TOL_L
+
+
+def test_deterministic_and_stream():
+    w = gen.custom(2, 4, 777, 777, 128, gen.BF16, True, 1.0, seed=42)
+    q, k, v = gen.make_qkv(w)
+    O1, L1 = run_cuda(w, q, k, v)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        O2, L2 = run_cuda(w, q, k, v, stream=s)
+    assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
+    assert torch.equal(L1, L2)
+
+
+def test_no_writes_outside_outputs():
+    """O and L are written exactly in [0, B*H*Nq*d) and [0, B*H*Nq): guard regions after
+    them keep their sentinel values."""
+    import exact_attention_forward_02_gb300 as fa
+    w = gen.custom(1, 3, 300, 257, 64, gen.F16, False, 1.0, seed=5)
+    q, k, v = gen.make_qkv(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    n_o = w.B * w.H * w.Nq * w.d
+    n_l = w.B * w.H * w.Nq
+    Obuf = torch.full((n_o + 8192,), 7.0, dtype=torch.float16, device=dev)
+    Lbuf = torch.full((n_l + 4096,), 7.0, dtype=torch.float32, device=dev)
+    rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), Obuf.data_ptr(), Lbuf.data_ptr(),
+                   w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, fa.FA_F16,
+                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert fa.fa_last_status() == 0
+    assert torch.all(Obuf[n_o:] == 7.0) and torch.all(Lbuf[n_l:] == 7.0)
+    assert not torch.any(Obuf[:n_o] == 7.0)
+
+
+def test_argument_errors_on_device_pointers():
+    import exact_attention_forward_02_gb300 as fa
+    dev = torch.device("cuda:0")
+    x = torch.zeros(4 * 128 * 64 + 64, dtype=torch.float16, device=dev)
+    Lb = torch.zeros(1024, dtype=torch.float32, device=dev)
+    p = x.data_ptr()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert fa.fa_fwd(p + 2, p, p, p, Lb.data_ptr(), 1, 1, 128, 128, 64, 0.125, 0, 0, st) == fa.FA_ERR_ALIGN
+    assert fa.fa_fwd(p, p, p, p, Lb.data_ptr() + 2, 1, 1, 128, 128, 64, 0.125, 0, 0, st) == fa.FA_ERR_ALIGN
+    assert fa.fa_fwd(p, p, p, p, Lb.data_ptr(), 1, 1, 128, 0, 64, 0.125, 0, 0, st) == fa.FA_ERR_EMPTY_KEYS
+    assert fa.fa_fwd(p, p, p, p, Lb.data_ptr(), 1, 1, 128, 128, 96, 0.125, 0, 0, st) == fa.FA_ERR_HEAD_DIM
+    assert fa.fa_fwd(p, p, p, p, Lb.data_ptr(), 1, 1, 128, 128, 64, float("nan"), 0, 0, st) == fa.FA_ERR_SCALE
+    torch.cuda.synchronize()
+    assert fa.fa_last_status() == 0
+
+
+def test_bounded_wait_times_out_cleanly_and_context_survives():
+    """A pipeline wait on a barrier that nothing signals gives up after its limit,
+    records FA_ERR_TIMEOUT, and the context stays usable for the next launch."""
+    import exact_attention_forward_02_gb300 as fa
+    assert fa.fa_clear_status() == 0
+    assert fa.fa_selftest_wait_timeout(2000) == 0
+    assert fa.fa_last_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_clear_status() == 0
+    assert fa.fa_last_status() == 0
+    r = _full_case(gen.WORKLOADS["tiny_causal"])
+    assert r["raw_ok"], r
