@@ -10,18 +10,19 @@
 //     O~   = exp(m - m') O~ + P V_j
 // and finally O = O~ / l, L = m + ln l. The scores never leave the SM.
 //
-// GB300 mapping (one persistent CTA per SM, 10 warps):
+// GB300 mapping (one persistent CTA per SM, 11 warps):
 //   warp 8      TMA producer: loads the two 128-row Q tiles of a work item once, then
 //               streams K_j, V_j through a ring of shared-memory slots (mbarrier pipeline).
-//   warp 9      MMA issuer: one thread issues tcgen05.mma for S = Q K^T (both operands
-//               K-major in shared memory, fp32 accumulator in Tensor Memory) and for
-//               O~ += P V (P from shared memory or Tensor Memory, V MN-major in shared
-//               memory), and signals completion with tcgen05.commit.
+//   warps 9,10  MMA issuers, one per Q tile: one thread each issues tcgen05.mma for
+//               S = Q K^T (both operands K-major in shared memory, fp32 accumulator in
+//               Tensor Memory) and O~ += P V (P read from Tensor Memory, V MN-major in
+//               shared memory), and signals completion with tcgen05.commit.
 //   warps 0-7   two softmax warpgroups, one per Q tile (ping-pong): thread r owns query
 //               row r of its tile (TMEM lane r), reads its 128 scores with tcgen05.ld,
 //               applies the mask, keeps (m, l) in registers in base-2 units (the scale is
-//               folded with log2(e)), writes P as 16-bit values, rescales O~ in TMEM when
-//               the running max grows by more than 2^8, and runs the epilogue.
+//               folded with log2(e)), writes P as 16-bit values over its scores in Tensor
+//               Memory, rescales O~ in TMEM when the running max grows by more than 2^8,
+//               and runs the epilogue.
 // Work items are (batch*head, 256-row query block); causal items run heaviest first.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,10 +35,6 @@
 #include "fa_fwd.h"
 #include "sm103_ptx.cuh"
 
-#ifndef FA_P_IN_TMEM
-#define FA_P_IN_TMEM 1
-#endif
-
 // Device-side status word (one per device that loads the library).
 __device__ int g_fa_status;
 
@@ -48,7 +45,7 @@ constexpr int BN = 128;                  // keys per K/V tile
 constexpr int NUM_WARPS = 10;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int WARP_LOAD = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA = 9;              // issues every MMA and owns the TMEM allocation
 constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O0 | O1, 128 columns each
 constexpr uint32_t TMEM_S0 = 0, TMEM_O0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O~ only when m grows > 2^8
@@ -57,26 +54,25 @@ constexpr int MAX_SLOTS = 8;
 
 struct Barriers {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[MAX_SLOTS], kv_empty[MAX_SLOTS];
+  uint64_t kv_full[MAX_SLOTS];
+  uint64_t kv_release[MAX_SLOTS];  // release unit m = {V of tile m-1, K of tile m}
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-template <int D, bool P_TMEM>
+template <int D>
 struct Layout {
   static constexpr int TILE_BYTES = BM * D * 2;       // one Q, K or V tile
   static constexpr int CHUNK_BYTES = BM * 128;        // 128 rows x one 128-byte swizzle span
   static constexpr int CHUNKS = D / 64;               // 64 16-bit elements per span
-  static constexpr int P_BYTES = P_TMEM ? 0 : BM * BN * 2;
-  static constexpr int FIXED = 2 * TILE_BYTES + 2 * P_BYTES + 1024 /*align*/ + 512 /*bars*/;
+  static constexpr int FIXED = 2 * TILE_BYTES + 1024 /*align*/ + 512 /*bars*/;
   static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TILE_BYTES;
   static constexpr int KV_SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;
-  static constexpr int OFF_P = OFF_KV + KV_SLOTS * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + KV_SLOTS * TILE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(Barriers) + 1024;
   static_assert(KV_SLOTS >= 2, "need at least two K/V slots");
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
@@ -133,6 +129,15 @@ struct Item {
   bool has1;  // the second 128-row tile holds at least one valid query row
 };
 
+// The r-th work item of this CTA. Items are ordered by decreasing cost (causal) and
+// dealt out boustrophedon: CTA b takes b, 2G-1-b, 2G+b, 4G-1-b, ... so that every CTA
+// gets one item from each "row" of G items, alternating heavy and light ends.
+__device__ __forceinline__ int item_of(int r, const Params& p) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int base = r * G;
+  return base + ((r & 1) ? (G - 1 - b) : b);
+}
+
 template <bool CAUSAL>
 __device__ __forceinline__ Item decode_item(int t, const Params& p) {
   Item it;
@@ -156,18 +161,17 @@ __device__ __forceinline__ Item decode_item(int t, const Params& p) {
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int D, bool BF16, bool CAUSAL, bool P_TMEM>
+template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using LY = Layout<D, P_TMEM>;
+  using LY = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + LY::OFF_BAR);
   const uint32_t sQ = smem_u32(smem + LY::OFF_Q);
   const uint32_t sKV = smem_u32(smem + LY::OFF_KV);
-  const uint32_t sP = smem_u32(smem + LY::OFF_P);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -178,11 +182,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(smem_u32(&bars->q_empty), 1);
     for (int s = 0; s < LY::KV_SLOTS; ++s) {
       mbar_init(smem_u32(&bars->kv_full[s]), 1);
-      mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+      mbar_init(smem_u32(&bars->kv_release[s]), 1);
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(smem_u32(&bars->s_full[g]), 1);
-      mbar_init(smem_u32(&bars->p_full[g]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&bars->p_full[g]), 4);    // one arrival per softmax warp
       mbar_init(smem_u32(&bars->o_done[g]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
@@ -209,24 +213,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
       const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t slot = 0, ph = 0, q_ph = 0;
+      // K/V loads are numbered globally (K_0 V_0 K_1 V_1 ... over all items of this CTA);
+      // load i goes to slot i mod KV_SLOTS. The slot's previous occupant (load i - KV_SLOTS)
+      // belongs to release unit u = (i - KV_SLOTS + 1) / 2, whose barrier is kv_release[u mod
+      // KV_SLOTS] at phase u / KV_SLOTS.
+      uint32_t ld = 0, q_ph = 0;
       uint32_t issued_mask = 0, last_par = 0;  // for draining on abort
       bool q_issued = false;
       bool ok = true;
       auto load_kv = [&](const CUtensorMap* tm, int bh, int row0) -> bool {
+        const uint32_t slot = ld % LY::KV_SLOTS;
+        const uint32_t par = (ld / LY::KV_SLOTS) & 1u;
+        if (ld >= (uint32_t)LY::KV_SLOTS) {
+          const uint32_t u = (ld - LY::KV_SLOTS + 1) >> 1;
+          if (!wait_bar(smem_u32(&bars->kv_release[u % LY::KV_SLOTS]), (u / LY::KV_SLOTS) & 1u,
+                        abort_flag, lim))
+            return false;
+        }
         const uint32_t full = smem_u32(&bars->kv_full[slot]);
-        if (!wait_bar(smem_u32(&bars->kv_empty[slot]), ph ^ 1, abort_flag, lim)) return false;
         mbar_arrive_expect_tx(full, LY::TILE_BYTES);
         const uint32_t dst = sKV + slot * LY::TILE_BYTES;
 #pragma unroll
         for (int c = 0; c < LY::CHUNKS; ++c)
           tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, tm, full, c * 64, row0, bh, pol_kv);
         issued_mask |= 1u << slot;
-        last_par = (last_par & ~(1u << slot)) | (ph << slot);
-        if (++slot == LY::KV_SLOTS) { slot = 0; ph ^= 1; }
+        last_par = (last_par & ~(1u << slot)) | (par << slot);
+        ++ld;
         return true;
       };
-      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      for (int r = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++r, p)) {
         const Item it = decode_item<CAUSAL>(t, p);
         ok = load_kv(&tmK, it.bh, 0);
         if (!ok) break;
@@ -264,46 +279,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BM, BN);
       constexpr uint32_t ID_O = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BM, D);
-      uint32_t slot = 0, ph = 0, q_ph = 0;
+      // descriptors are built once; per k-step and per slot only the start-address field
+      // (bits 0-13, in 16-byte units) advances, which never carries out of its field
+      const uint64_t dQ0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dK = umma_smem_desc(sKV, 16, 1024);
+      const uint64_t dV = umma_smem_desc(sKV, LY::CHUNK_BYTES, 1024);
+      uint32_t m = 0;  // global K/V tile counter: K_m is load 2m, V_m is load 2m+1
+      uint32_t q_ph = 0;
       uint32_t p_ph[2] = {0, 0};
       bool ok = true;
-      auto take = [&](uint32_t& s_out, uint32_t& ph_out) {
-        s_out = slot;
-        ph_out = ph;
-        if (++slot == LY::KV_SLOTS) { slot = 0; ph ^= 1; }
+      auto kv_wait = [&](uint32_t ld, uint32_t& slot) -> bool {
+        slot = ld % LY::KV_SLOTS;
+        return wait_bar(smem_u32(&bars->kv_full[slot]), (ld / LY::KV_SLOTS) & 1u, abort_flag, lim);
       };
       // S_g = Q_g K^T : M=128 rows, N=128 keys, K=D (16 per instruction)
       auto issue_s = [&](int g, uint32_t kslot) {
-        const uint32_t qa = sQ + g * LY::TILE_BYTES;
-        const uint32_t ka = sKV + kslot * LY::TILE_BYTES;
+        const uint64_t dq = dQ0 + ((g * LY::TILE_BYTES) >> 4);
+        const uint64_t dk = dK + ((kslot * LY::TILE_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32;
-          umma_ss(tmem + TMEM_S0 + g * 128, umma_smem_desc(qa + off, 16, 1024),
-                  umma_smem_desc(ka + off, 16, 1024), ID_S, ks > 0 ? 1u : 0u);
+          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
         }
       };
-      // O_g += P_g V : M=128 rows, N=D, K=128 keys
+      // O_g += P_g V : M=128 rows, N=D, K=128 keys; P is read from Tensor Memory
       auto issue_pv = [&](int g, uint32_t vslot, bool acc) {
-        const uint32_t va = sKV + vslot * LY::TILE_BYTES;
+        const uint64_t dv = dV + ((vslot * LY::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bdesc = umma_smem_desc(va + ks * 16 * 128, LY::CHUNK_BYTES, 1024);
-          const uint32_t accf = (acc || ks > 0) ? 1u : 0u;
-          if constexpr (P_TMEM) {
-            umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8, bdesc, ID_O, accf);
-          } else {
-            const uint32_t pa = sP + g * LY::P_BYTES + (ks >> 2) * (BM * 128) + (ks & 3) * 32;
-            umma_ss(tmem + TMEM_O0 + g * 128, umma_smem_desc(pa, 16, 1024), bdesc, ID_O, accf);
-          }
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
+                  dv + ((ks * 16 * 128) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
       };
-      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      for (int r = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++r, p)) {
         const Item it = decode_item<CAUSAL>(t, p);
-        uint32_t sK, phK;
-        take(sK, phK);
-        ok = wait_bar(smem_u32(&bars->kv_full[sK]), phK, abort_flag, lim) &&
-             wait_bar(smem_u32(&bars->q_full), q_ph, abort_flag, lim);
+        uint32_t sK;
+        ok = kv_wait(2 * m, sK) && wait_bar(smem_u32(&bars->q_full), q_ph, abort_flag, lim);
         if (!ok) break;
         q_ph ^= 1;
         tc_fence_after();
@@ -313,26 +323,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           issue_s(1, sK);
           umma_commit(smem_u32(&bars->s_full[1]));
         }
-        umma_commit(smem_u32(&bars->kv_empty[sK]));
+        umma_commit(smem_u32(&bars->kv_release[m % LY::KV_SLOTS]));
         for (int j = 0; j < it.n_kv; ++j) {
-          uint32_t sV, phV, sKn = 0, phKn = 0;
-          take(sV, phV);
+          const uint32_t mj = m + j;
           const bool has_next = j + 1 < it.n_kv;
-          if (has_next) take(sKn, phKn);
-          ok = wait_bar(smem_u32(&bars->kv_full[sV]), phV, abort_flag, lim) &&
-               wait_bar(smem_u32(&bars->p_full[0]), p_ph[0], abort_flag, lim);
+          uint32_t sV, sKn = 0;
+          ok = kv_wait(2 * mj + 1, sV) && wait_bar(smem_u32(&bars->p_full[0]), p_ph[0], abort_flag, lim);
           if (!ok) break;
           p_ph[0] ^= 1;
           tc_fence_after();
           issue_pv(0, sV, j > 0);
-          umma_commit(smem_u32(&bars->o_done[0]));
-          if (!it.has1) umma_commit(smem_u32(&bars->kv_empty[sV]));
           if (has_next) {
-            ok = wait_bar(smem_u32(&bars->kv_full[sKn]), phKn, abort_flag, lim);
+            // S_g(j+1) is issued after PV_g(j): its commit also tells the softmax warps
+            // that O_g is up to date (tcgen05 ops of one thread complete in issue order)
+            ok = kv_wait(2 * mj + 2, sKn);
             if (!ok) break;
             tc_fence_after();
             issue_s(0, sKn);
             umma_commit(smem_u32(&bars->s_full[0]));
+          } else {
+            umma_commit(smem_u32(&bars->o_done[0]));
           }
           if (it.has1) {
             ok = wait_bar(smem_u32(&bars->p_full[1]), p_ph[1], abort_flag, lim);
@@ -340,18 +350,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             p_ph[1] ^= 1;
             tc_fence_after();
             issue_pv(1, sV, j > 0);
-            umma_commit(smem_u32(&bars->o_done[1]));
-            umma_commit(smem_u32(&bars->kv_empty[sV]));
             if (has_next) {
               issue_s(1, sKn);
               umma_commit(smem_u32(&bars->s_full[1]));
+            } else {
+              umma_commit(smem_u32(&bars->o_done[1]));
             }
           }
-          if (has_next) umma_commit(smem_u32(&bars->kv_empty[sKn]));
+          // unit mj+1 = {V_mj, K_mj+1}: both are consumed once the MMAs above complete
+          if (has_next) umma_commit(smem_u32(&bars->kv_release[(mj + 1) % LY::KV_SLOTS]));
         }
+        m += it.n_kv;
         if (ok) umma_commit(smem_u32(&bars->q_empty));
       }
-      // make sure every issued MMA has finished before TMEM can be released
+      // every issued MMA must finish before TMEM can be released
       umma_commit(smem_u32(&bars->mma_drain));
       wait_drain(smem_u32(&bars->mma_drain), 0, lim);
     }
@@ -366,21 +378,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float c = p.c;
     uint32_t s_ph = 0, o_ph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+    for (int rr = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++rr, p)) {
       const Item it = decode_item<CAUSAL>(t, p);
       if (g == 1 && !it.has1) continue;
       const int row = it.q0 + g * BM + r;
       const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, kv_lim) visible
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < it.n_kv; ++j) {
-        bool w = wait_bar(smem_u32(&bars->s_full[g]), s_ph, abort_flag, lim);
-        if (j > 0 && w) w = wait_bar(smem_u32(&bars->o_done[g]), o_ph, abort_flag, lim);
-        ok = __all_sync(0xffffffffu, w);
+        // S_g(j) ready; for j > 0 this also means PV_g(j-1) has completed
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full[g]), s_ph, abort_flag, lim));
         if (!ok) break;
         s_ph ^= 1;
-        if (j > 0) o_ph ^= 1;
         tc_fence_after();
-
         uint32_t sr[4][32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
@@ -458,29 +467,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         l_run = l_run * alpha + ls;
         m_run = m_new;
 
-        if constexpr (P_TMEM) {
-          // P overwrites the first 64 columns of this tile's S region
-          tmem_st32(tS, pk[0]);
-          tmem_st32(tS + 32, pk[1]);
-          tmem_wait_st();
-        } else {
-          tmem_wait_st();
-          // K-major tile with the 128-byte swizzle: row r at r*128 within each 64-key
-          // span, 16-byte unit u stored at unit (u ^ (r mod 8))
-          const uint32_t prow = sP + g * LY::P_BYTES + r * 128;
-          const uint32_t sw = (uint32_t)(r & 7);
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t addr = prow + cc * (BM * 128) + ((u ^ sw) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[cc][u * 4]),
-                           "r"(pk[cc][u * 4 + 1]), "r"(pk[cc][u * 4 + 2]), "r"(pk[cc][u * 4 + 3])
-                           : "memory");
-            }
-          }
-          fence_proxy_async_smem();
-        }
+        // P overwrites the first 64 columns of this tile's S region (the A operand of PV)
+        tmem_st32(tS, pk[0]);
+        tmem_st32(tS + 32, pk[1]);
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[g]));
@@ -617,9 +607,8 @@ int device_info(DeviceInfo** out) {
 template <int D, bool BF16, bool CAUSAL>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
            DeviceInfo* di, cudaStream_t st) {
-  constexpr bool PT = FA_P_IN_TMEM != 0;
-  using LY = Layout<D, PT>;
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, PT>;
+  using LY = Layout<D>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     bool& set = di->attr_set[D == 128][BF16][CAUSAL];

@@ -74,7 +74,12 @@ def test_small_full_compare(case):
     w = gen.custom(B, H, Nq, Nk, d, dt, causal, std, seed=1000 + sum(case[:5]))
     r = _full_case(w, v_std=1.0)
     print(w.describe(), r)
-    assert r["raw_ok"], r
+    assert r["graded_ok"], r
+    if std == 1.0:
+        # unit-variance inputs meet the plain bound; a sharp softmax (large Q, K) may add
+        # the rounding of P to 16 bits on top of the output rounding, which the graded
+        # bound (tolerance + half an ulp of the exact output) still holds
+        assert r["raw_ok"], r
 
 
 @pytest.mark.parametrize("name", ["tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross"])
