@@ -42,10 +42,14 @@ namespace fa {
 
 constexpr int BM = 128;                  // query rows per tile = TMEM lanes
 constexpr int BN = 128;                  // keys per K/V tile
-constexpr int NUM_WARPS = 10;
+constexpr int NUM_WARPS = 12;            // three warpgroups: softmax 0, softmax 1, load/MMA
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int WARP_LOAD = 8;
 constexpr int WARP_MMA = 9;              // issues every MMA and owns the TMEM allocation
+// Register split (launch: 384 threads x 168): the load/MMA warpgroup gives registers
+// to the two softmax warpgroups: 2*128*200 + 128*104 = 64512 = 384*168.
+constexpr uint32_t REGS_SOFTMAX = 200;
+constexpr uint32_t REGS_OTHER = 104;
 constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O0 | O1, 128 columns each
 constexpr uint32_t TMEM_S0 = 0, TMEM_O0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O~ only when m grows > 2^8
@@ -90,7 +94,7 @@ struct Params {
 };
 
 // ----------------------------------------------------------------------------- waits
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        unsigned long long limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -106,7 +110,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
   }
 }
 // Drain wait used on the way out after an abort: ignores the abort flag, still bounded.
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > limit_ns) {
@@ -207,7 +211,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const unsigned long long lim = p.wait_limit_ns;
-
+  if (warp >= WARP_LOAD) {
+  regs_dec<REGS_OTHER>();
   if (warp == WARP_LOAD) {
     // ======================================================================= producer
     if (lane == 0) {
@@ -276,7 +281,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == WARP_MMA) {
     // ======================================================================= MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged, so descriptors and counters stay
+    // warp-uniform; one elected lane issues each tcgen05.mma / commit.
+    {
       constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BM, BN);
       constexpr uint32_t ID_O = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BM, D);
       // descriptors are built once; per k-step and per slot only the start-address field
@@ -288,47 +295,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t q_ph = 0;
       uint32_t p_ph[2] = {0, 0};
       bool ok = true;
+      auto wait_all = [&](uint32_t bar, uint32_t par) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+      };
       auto kv_wait = [&](uint32_t ld, uint32_t& slot) -> bool {
         slot = ld % LY::KV_SLOTS;
-        return wait_bar(smem_u32(&bars->kv_full[slot]), (ld / LY::KV_SLOTS) & 1u, abort_flag, lim);
+        return wait_all(smem_u32(&bars->kv_full[slot]), (ld / LY::KV_SLOTS) & 1u);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (elect_one()) umma_commit(smem_u32(bar));
+        __syncwarp();
       };
       // S_g = Q_g K^T : M=128 rows, N=128 keys, K=D (16 per instruction)
       auto issue_s = [&](int g, uint32_t kslot) {
         const uint64_t dq = dQ0 + ((g * LY::TILE_BYTES) >> 4);
         const uint64_t dk = dK + ((kslot * LY::TILE_BYTES) >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
-          umma_ss(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+          }
         }
+        __syncwarp();
       };
       // O_g += P_g V : M=128 rows, N=D, K=128 keys; P is read from Tensor Memory
       auto issue_pv = [&](int g, uint32_t vslot, bool acc) {
         const uint64_t dv = dV + ((vslot * LY::TILE_BYTES) >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
-                  dv + ((ks * 16 * 128) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
+                    dv + ((ks * 16 * 128) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+        }
+        __syncwarp();
       };
       for (int r = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++r, p)) {
         const Item it = decode_item<CAUSAL>(t, p);
         uint32_t sK;
-        ok = kv_wait(2 * m, sK) && wait_bar(smem_u32(&bars->q_full), q_ph, abort_flag, lim);
+        ok = kv_wait(2 * m, sK) && wait_all(smem_u32(&bars->q_full), q_ph);
         if (!ok) break;
         q_ph ^= 1;
         tc_fence_after();
         issue_s(0, sK);
-        umma_commit(smem_u32(&bars->s_full[0]));
+        commit(&bars->s_full[0]);
         if (it.has1) {
           issue_s(1, sK);
-          umma_commit(smem_u32(&bars->s_full[1]));
+          commit(&bars->s_full[1]);
         }
-        umma_commit(smem_u32(&bars->kv_release[m % LY::KV_SLOTS]));
+        commit(&bars->kv_release[m % LY::KV_SLOTS]);
         for (int j = 0; j < it.n_kv; ++j) {
           const uint32_t mj = m + j;
           const bool has_next = j + 1 < it.n_kv;
           uint32_t sV, sKn = 0;
-          ok = kv_wait(2 * mj + 1, sV) && wait_bar(smem_u32(&bars->p_full[0]), p_ph[0], abort_flag, lim);
+          ok = kv_wait(2 * mj + 1, sV) && wait_all(smem_u32(&bars->p_full[0]), p_ph[0]);
           if (!ok) break;
           p_ph[0] ^= 1;
           tc_fence_after();
@@ -340,34 +360,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             issue_s(0, sKn);
-            umma_commit(smem_u32(&bars->s_full[0]));
+            commit(&bars->s_full[0]);
           } else {
-            umma_commit(smem_u32(&bars->o_done[0]));
+            commit(&bars->o_done[0]);
           }
           if (it.has1) {
-            ok = wait_bar(smem_u32(&bars->p_full[1]), p_ph[1], abort_flag, lim);
+            ok = wait_all(smem_u32(&bars->p_full[1]), p_ph[1]);
             if (!ok) break;
             p_ph[1] ^= 1;
             tc_fence_after();
             issue_pv(1, sV, j > 0);
             if (has_next) {
               issue_s(1, sKn);
-              umma_commit(smem_u32(&bars->s_full[1]));
+              commit(&bars->s_full[1]);
             } else {
-              umma_commit(smem_u32(&bars->o_done[1]));
+              commit(&bars->o_done[1]);
             }
           }
           // unit mj+1 = {V_mj, K_mj+1}: both are consumed once the MMAs above complete
-          if (has_next) umma_commit(smem_u32(&bars->kv_release[(mj + 1) % LY::KV_SLOTS]));
+          if (has_next) commit(&bars->kv_release[(mj + 1) % LY::KV_SLOTS]);
         }
         m += it.n_kv;
-        if (ok) umma_commit(smem_u32(&bars->q_empty));
+        if (ok) commit(&bars->q_empty);
       }
       // every issued MMA must finish before TMEM can be released
-      umma_commit(smem_u32(&bars->mma_drain));
+      commit(&bars->mma_drain);
       wait_drain(smem_u32(&bars->mma_drain), 0, lim);
+      __syncwarp();
     }
+  }
+  // exit: every role of the CTA has finished with Tensor Memory
+  tc_fence_before();
+  named_bar_sync(1, NUM_THREADS);
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
   } else {
+    regs_inc<REGS_SOFTMAX>();
     // ======================================================================= softmax
     const int g = warp >> 2;         // which Q tile / warpgroup
     const int wq = warp & 3;         // TMEM lane quarter this warp may access
@@ -397,21 +427,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         const int vis = kv_lim - j * BN;
         const bool full = vis >= BN;
-        // raw row max over visible keys
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        auto sv = [&](int k) { return __uint_as_float(sr[k >> 5][k & 31]); };
+        // raw row max over the visible keys (three-input max, four chains)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (full) {
 #pragma unroll
-          for (int k = 0; k < 128; ++k)
-            mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(sr[k >> 5][k & 31]));
+          for (int k = 0; k < 64; ++k) mx[k & 3] = max3(mx[k & 3], sv(2 * k), sv(2 * k + 1));
         } else {
 #pragma unroll
-          for (int k = 0; k < 128; ++k)
-            mx[k & 7] = fmaxf(mx[k & 7], k < vis ? __uint_as_float(sr[k >> 5][k & 31]) : -INFINITY);
+          for (int k = 0; k < 64; ++k)
+            mx[k & 3] = max3(mx[k & 3], 2 * k < vis ? sv(2 * k) : -INFINITY,
+                             2 * k + 1 < vis ? sv(2 * k + 1) : -INFINITY);
         }
-        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
         const float m_tile = (mt == -INFINITY) ? -INFINITY : mt * c;
         float m_new = m_run, alpha = 1.f;
         bool rescale = false;
@@ -423,44 +451,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           rescale = true;
         }
         const float nb = (m_new == -INFINITY) ? 0.f : -m_new;
-        float sum[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sum[i] = 0.f;
-        // P = exp2(S*c - m) in fp32 for the row sum, packed to 16-bit pairs (key 2k in
-        // the low half, key 2k+1 in the high half) for the second product
+        // P = exp2(S*c - m): the scaling in packed pairs, the exponentials on the MUFU,
+        // the row sum in packed pairs; P is packed to 16-bit pairs (key 2k in the low
+        // half, key 2k+1 in the high half) for the second product
+        const uint64_t c2 = f2(c, c), nb2 = f2(nb, nb);
+        uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[2][32];
-        if (full) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[(2 * k) >> 5][(2 * k) & 31]), c, nb));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[(2 * k + 1) >> 5][(2 * k + 1) & 31]), c, nb));
-            sum[(2 * k) & 7] += p0;
-            sum[(2 * k + 1) & 7] += p1;
-            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+        for (int k = 0; k < 64; ++k) {
+          float t0, t1;
+          f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
+          float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          if (!full) {
+            p0 = 2 * k < vis ? p0 : 0.f;
+            p1 = 2 * k + 1 < vis ? p1 : 0.f;
           }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const float p0 = (2 * k < vis)
-                ? ex2_approx(fmaf(__uint_as_float(sr[(2 * k) >> 5][(2 * k) & 31]), c, nb)) : 0.f;
-            const float p1 = (2 * k + 1 < vis)
-                ? ex2_approx(fmaf(__uint_as_float(sr[(2 * k + 1) >> 5][(2 * k + 1) & 31]), c, nb)) : 0.f;
-            sum[(2 * k) & 7] += p0;
-            sum[(2 * k + 1) & 7] += p1;
-            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
-          }
+          acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
+          pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
         }
-        const float ls = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+        float ls;
+        {
+          float a0, a1, b0, b1;
+          f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+          (void)b0; (void)b1;
+          ls = a0 + a1;
+        }
 
         // rescale O~ (in TMEM) when this row's max grew past the threshold
         if (__any_sync(0xffffffffu, rescale)) {
+          const uint64_t al2 = f2(alpha, alpha);
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             tmem_ld32(tO + q * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            for (int k = 0; k < 16; ++k) {
+              float x0, x1;
+              f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2), x0, x1);
+              o[2 * k] = __float_as_uint(x0);
+              o[2 * k + 1] = __float_as_uint(x1);
+            }
             tmem_st32(tO + q * 32, o);
           }
         }
@@ -493,9 +524,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tO + q * 32, o);
           tmem_wait_ld();
           uint32_t w16[16];
+          const uint64_t il2 = f2(inv_l, inv_l);
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+          for (int k = 0; k < 16; ++k) {
+            float x0, x1;
+            f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), il2), x0, x1);
+            w16[k] = pack2<BF16>(x0, x1);
+          }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
 #pragma unroll
@@ -507,13 +542,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
       }
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == WARP_MMA) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    // exit: the load/MMA warpgroup releases Tensor Memory after this barrier
+    tc_fence_before();
+    named_bar_sync(1, NUM_THREADS);
   }
 }
 
