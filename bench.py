@@ -45,6 +45,22 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max_over_ranks(values):
+    """Element-wise maximum of `values` over all ranks (identity on one process)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(flops_per_rank_step: float, world: int, step_ms_max: float) -> float:
+    """Replicas: every rank runs the same step; the job's rate is all ranks' FLOPs over the
+    slowest rank's step time."""
+    return world * flops_per_rank_step / (step_ms_max * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -63,7 +79,7 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic():
+def recorded_traffic(workload):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, only
     while the kernel source is the one those counters were taken on."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -72,7 +88,7 @@ def recorded_traffic():
             rec = json.load(f)
         if rec.get("source_sha256") != kernel_source_hash():
             return None
-        return rec["kernels"][DOMINANT]["dram_bytes_per_launch"]
+        return rec["kernels"][workload]["dram_bytes_per_launch"]
     except Exception:
         return None
 
@@ -167,7 +183,8 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
 
-    wl = [gen.WORKLOADS[n] for n in WORKLOADS]
+    names = tuple(args.workloads.split(",")) if args.workloads else WORKLOADS
+    wl = [gen.WORKLOADS[n] for n in names]
     host = {}
     devbuf = {}
     for w in wl:
@@ -182,7 +199,8 @@ def run_ours(args):
     def launch(w):
         qd, kd, vd, O, L = devbuf[w.name]
         rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(), L.data_ptr(),
-                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, fa.FA_BF16, sp)
+                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal,
+                       fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16, sp)
         if rc != 0:
             raise fa.FAError(rc)
 
@@ -231,7 +249,7 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, launch, D2H O and L
     ne2e = max(3, min(n, 50))
-    pin_out = {w.name: (torch.empty((w.B, w.H, w.Nq, w.d), dtype=torch.bfloat16).pin_memory(),
+    pin_out = {w.name: (torch.empty((w.B, w.H, w.Nq, w.d), dtype=gen.torch_dtype(w.dtype)).pin_memory(),
                         torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()) for w in wl}
     h2d = sum(t.numel() * t.element_size() for w in wl for t in host[w.name])
     d2h = sum(t.numel() * t.element_size() for w in wl for t in pin_out[w.name])
@@ -257,18 +275,16 @@ def run_ours(args):
     e2e_s = time.perf_counter() - t0
 
     # ---- max over ranks
-    times = torch.tensor([step_ms, e2e_s / ne2e * 1e3, t_wall], dtype=torch.float64)
-    if ws > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    step_ms_max, e2e_ms_max, wall_max = times.tolist()
+    step_ms_max, e2e_ms_max, wall_max = reduce_max_over_ranks([step_ms, e2e_s / ne2e * 1e3, t_wall])
 
     if rank == 0:
         peak, peak_sus, peak_kind = peaks()
-        wd = gen.WORKLOADS[DOMINANT]
-        dom_ms = statistics.fmean(per[DOMINANT])
+        dominant = DOMINANT if DOMINANT in per else max(per, key=lambda n: statistics.fmean(per[n]))
+        wd = gen.WORKLOADS[dominant]
+        dom_ms = statistics.fmean(per[dominant])
         achieved = wd.flops / (dom_ms * 1e-3) / 1e12
         clk = clocks.summary() if clocks else None
-        value = ws * flops_step / (step_ms_max * 1e-3) / 1e12
+        value = whole_job_tflops(flops_step, ws, step_ms_max)
         breakdown = {}
         for w in wl:
             ms = statistics.fmean(per[w.name])
@@ -280,21 +296,22 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "+".join(WORKLOADS),
+            "dtype": "+".join(sorted({w.dtype for w in wl})), "data": "synthetic",
+            "config": {"workload": "+".join(names),
                        "shapes": [w.describe() for w in wl],
                        "l2": "flushed before every launch (256 MiB write, outside the events)",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
                        "pct_of_peak": round(100 * value / ws / peak, 1)},
             "breakdown": breakdown,
-            "roofline": {"bound": "tensor", "kernel": f"fa_fwd_kernel<128, bf16, causal> on {DOMINANT}",
+            "roofline": {"bound": "tensor",
+                         "kernel": f"fa_fwd_kernel<{wd.d}, {wd.dtype}, {'causal' if wd.causal else 'full'}> on {dominant}",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} bf16 dense (burst: kernel timed alone)",
-                         "traffic": recorded_traffic(),
+                         "traffic": recorded_traffic(dominant),
                          "algorithmic_bytes": wd.io_bytes},
             "clocks": clk,
-            "e2e": {"value": round(ws * flops_step / (e2e_ms_max * 1e-3) / 1e12, 2), "unit": UNIT,
+            "e2e": {"value": round(whole_job_tflops(flops_step, ws, e2e_ms_max), 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ne2e},
             "gpu_launches": int(launches),
             "wall_s_timed": round(wall_max, 4),
@@ -402,6 +419,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workloads", default="",
+                    help="comma-separated workload names (default: the two headline workloads)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of host time for the oracle CPU baseline (0 = skip)")
     args = ap.parse_args()

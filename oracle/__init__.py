@@ -64,6 +64,32 @@ def _load():
     return _lib
 
 
+class using_library:
+    """Context manager: run the wrappers of this module against another build of the
+    oracle (the mutation tests load deliberately broken copies this way)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._saved = _lib
+        lib = ctypes.CDLL(self.path)
+        for name in ("fa_oracle_hw_threads", "fa_oracle_attention", "fa_oracle_attention_rows",
+                     "fa_oracle_probs", "fa_oracle_online_softmax", "fa_oracle_merge",
+                     "fa_oracle_block_state"):
+            f, g = getattr(lib, name), getattr(self._saved, name)
+            f.restype, f.argtypes = g.restype, g.argtypes
+        _lib = lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
 def _f64(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
 

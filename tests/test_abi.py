@@ -1,0 +1,81 @@
+"""The C ABI library loads on a machine without a GPU, exports every function that
+include/*.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        # every function the header declares: "<type> name(" at the start of a statement
+        names += re.findall(r"^[A-Za-z_][\w \t\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_last_status" in names and "fa_strerror" in names, names
+
+
+def test_library_exports_every_declared_symbol():
+    import exact_attention_forward_02_gb300 as fa
+    lib = ctypes.CDLL(fa.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in include/*.h but not exported: {missing}"
+
+
+def test_status_strings():
+    import exact_attention_forward_02_gb300 as fa
+    for code, name in fa.STATUS.items():
+        assert fa.strerror(code) and "unknown" not in fa.strerror(code), name
+    assert "unknown" in fa.strerror(12345)
+
+
+# Host-side checks run before any CUDA call, so they work without a GPU. Fake pointers
+# (never dereferenced) stand in for device memory.
+P = 1 << 20  # 16-byte aligned, non-null, never touched
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1), "FA_ERR_NULL"),
+    ((P, P, P, P, 0, 1, 1, 128, 128, 64, 0.125, 0, 1), "FA_ERR_NULL"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 96, 0.125, 0, 1), "FA_ERR_HEAD_DIM"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 256, 0.125, 0, 1), "FA_ERR_HEAD_DIM"),
+    ((P, P, P, P, P, -1, 1, 128, 128, 64, 0.125, 0, 1), "FA_ERR_SHAPE"),
+    ((P, P, P, P, P, 1, 1, -5, 128, 64, 0.125, 0, 1), "FA_ERR_SHAPE"),
+    ((P, P, P, P, P, 1, 1, 128, -1, 64, 0.125, 0, 1), "FA_ERR_SHAPE"),
+    ((P, P, P, P, P, 1, 1, 128, 0, 64, 0.125, 0, 1), "FA_ERR_EMPTY_KEYS"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 64, float("nan"), 0, 1), "FA_ERR_SCALE"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 64, float("inf"), 0, 1), "FA_ERR_SCALE"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 64, -0.5, 0, 1), "FA_ERR_SCALE"),
+    ((P + 2, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1), "FA_ERR_ALIGN"),
+    ((P, P, P + 8, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1), "FA_ERR_ALIGN"),
+    ((P, P, P, P, P + 2, 1, 1, 128, 128, 64, 0.125, 0, 1), "FA_ERR_ALIGN"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 2), "FA_ERR_DTYPE"),
+    ((P, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, -1), "FA_ERR_DTYPE"),
+    ((P, P, P, P, P, 70000, 70000, 128, 128, 64, 0.125, 0, 1), "FA_ERR_SHAPE"),
+    # nothing to compute: success without touching the pointers (even NULL ones)
+    ((0, 0, 0, 0, 0, 0, 4, 128, 128, 64, 0.125, 0, 1), "FA_OK"),
+    ((0, 0, 0, 0, 0, 2, 4, 0, 128, 64, 0.125, 1, 1), "FA_OK"),
+    ((0, 0, 0, 0, 0, 2, 4, 0, 0, 128, 0.125, 1, 0), "FA_OK"),
+])
+def test_host_argument_checks(args, code):
+    import exact_attention_forward_02_gb300 as fa
+    *a, dt = args
+    rc = fa.fa_fwd(*a, dt, None)
+    assert rc == getattr(fa, code), (rc, fa.strerror(rc))
+
+
+def test_selftest_rejects_out_of_range_limit():
+    import exact_attention_forward_02_gb300 as fa
+    assert fa.fa_selftest_wait_timeout(0) == fa.FA_ERR_SHAPE
+    assert fa.fa_selftest_wait_timeout(2_000_000) == fa.FA_ERR_SHAPE
