@@ -457,17 +457,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t c2 = f2(c, c), nb2 = f2(nb, nb);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[2][32];
+        // two branch-free copies of the loop (full tile / masked tile) so that the
+        // scheduler can overlap the exponentials of many iterations
+        if (full) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          float t0, t1;
-          f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
-          float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-          if (!full) {
-            p0 = 2 * k < vis ? p0 : 0.f;
-            p1 = 2 * k + 1 < vis ? p1 : 0.f;
+          for (int k = 0; k < 64; ++k) {
+            float t0, t1;
+            f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
+            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
           }
-          acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
-          pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            float t0, t1;
+            f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
+            const float p0 = 2 * k < vis ? ex2_approx(t0) : 0.f;
+            const float p1 = 2 * k + 1 < vis ? ex2_approx(t1) : 0.f;
+            acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
+            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+          }
         }
         float ls;
         {
