@@ -424,6 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
         tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
 
         const int vis = kv_lim - j * BN;
         const bool full = vis >= BN;
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t o[32];
             tmem_ld32(tO + q * 32, o);
             tmem_wait_ld();
+            reg_fence(o);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               float x0, x1;
@@ -533,6 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t o[32];
           tmem_ld32(tO + q * 32, o);
           tmem_wait_ld();
+          reg_fence(o);
           uint32_t w16[16];
           const uint64_t il2 = f2(inv_l, inv_l);
 #pragma unroll
