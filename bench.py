@@ -193,14 +193,23 @@ def run_ours(args):
         qd, kd, vd = (t.to(dev) for t in (q, k, v))
         O = torch.empty((w.B, w.H, w.Nq, w.d), dtype=q.dtype, device=dev)
         L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
-        devbuf[w.name] = (qd, kd, vd, O, L)
+        # stream-K workspace for full attention (zero-filled once; calls keep it zeroed),
+        # only when --streamk asks for it
+        nws = fa.fa_fwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, w.causal) if args.streamk else 0
+        wsp = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev) if nws else None
+        devbuf[w.name] = (qd, kd, vd, O, L, wsp)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def launch(w):
-        qd, kd, vd, O, L = devbuf[w.name]
-        rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(), L.data_ptr(),
-                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal,
-                       fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16, sp)
+        qd, kd, vd, O, L, wsp = devbuf[w.name]
+        dt = fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16
+        if wsp is None:
+            rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(), L.data_ptr(),
+                           w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt, sp)
+        else:
+            rc = fa.fa_fwd_ws(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(),
+                              L.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt,
+                              wsp.data_ptr(), wsp.numel(), sp)
         if rc != 0:
             raise fa.FAError(rc)
 
@@ -256,7 +265,7 @@ def run_ours(args):
 
     def e2e_step():
         for w in wl:
-            qd, kd, vd, O, L = devbuf[w.name]
+            qd, kd, vd, O, L, _ = devbuf[w.name]
             for dst, src in zip((qd, kd, vd), host[w.name]):
                 dst.copy_(src, non_blocking=True)
             launch(w)
@@ -301,6 +310,7 @@ def run_ours(args):
                        "shapes": [w.describe() for w in wl],
                        "l2": "flushed before every launch (256 MiB write, outside the events)",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
+                       "entry_point": "fa_fwd_ws (stream-K)" if args.streamk else "fa_fwd",
                        "pct_of_peak": round(100 * value / ws / peak, 1)},
             "breakdown": breakdown,
             "roofline": {"bound": "tensor",
@@ -421,6 +431,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workloads", default="",
                     help="comma-separated workload names (default: the two headline workloads)")
+    ap.add_argument("--streamk", action="store_true",
+                    help="call fa_fwd_ws with a workspace (stream-K split of full attention)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of host time for the oracle CPU baseline (0 = skip)")
     args = ap.parse_args()

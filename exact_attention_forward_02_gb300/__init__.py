@@ -25,6 +25,7 @@ STATUS = {
     0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_HEAD_DIM", -3: "FA_ERR_SHAPE",
     -4: "FA_ERR_EMPTY_KEYS", -5: "FA_ERR_SCALE", -6: "FA_ERR_ALIGN", -7: "FA_ERR_DTYPE",
     -8: "FA_ERR_CUDA", -9: "FA_ERR_TENSOR_MAP", -10: "FA_ERR_DEVICE", -11: "FA_ERR_TIMEOUT",
+    -12: "FA_ERR_WORKSPACE",
 }
 globals().update({v: k for k, v in STATUS.items()})
 
@@ -45,6 +46,11 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_fwd_ws.restype = ctypes.c_int
+    lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int] * 6
     lib.fa_last_status.restype = ctypes.c_int
     lib.fa_last_status.argtypes = []
     lib.fa_clear_status.restype = ctypes.c_int
@@ -71,6 +77,19 @@ def fa_fwd(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream) -> int:
                           float(scale), int(bool(causal)), int(dtype), stream))
 
 
+def fa_fwd_ws(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, workspace, workspace_bytes,
+              stream) -> int:
+    """C-ABI call of the workspace variant (stream-K split of the key range)."""
+    return int(lib.fa_fwd_ws(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
+                             float(scale), int(bool(causal)), int(dtype), workspace,
+                             int(workspace_bytes), stream))
+
+
+def fa_fwd_workspace_bytes(B, H, Nq, Nk, d, causal) -> int:
+    return int(lib.fa_fwd_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(d),
+                                          int(bool(causal))))
+
+
 def fa_last_status() -> int:
     return int(lib.fa_last_status())
 
@@ -88,11 +107,13 @@ def fa_num_kernel_launches() -> int:
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-              stream=None):
+              stream=None, workspace=None):
     """O, L = attention(q, k, v) for CUDA tensors q [B,H,Nq,d], k/v [B,H,Nk,d] (fp16/bf16).
 
     Allocates O (like q) and L ([B,H,Nq] fp32) unless given; launches on `stream`
     (a torch.cuda.Stream, default: the current stream) and returns without synchronising.
+    `workspace`: a zero-filled uint8 CUDA tensor of at least fa_fwd_workspace_bytes(...)
+    bytes enables the stream-K split for full attention (see include/fa_fwd.h).
     """
     import torch
 
@@ -119,8 +140,14 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         stream = torch.cuda.current_stream(q.device)
     dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_F16
     with torch.cuda.device(q.device):
-        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                    B, H, Nq, Nk, d, scale, causal, dt, ctypes.c_void_p(stream.cuda_stream))
+        if workspace is None:
+            rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, H, Nq, Nk, d, scale, causal, dt, ctypes.c_void_p(stream.cuda_stream))
+        else:
+            rc = fa_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, Nq, Nk, d, scale, causal, dt,
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                           ctypes.c_void_p(stream.cuda_stream))
     if rc != 0:
         raise FAError(rc)
     return out, lse

@@ -91,6 +91,11 @@ struct Params {
   int n_kv_all;    // ceil(Nk / 128)
   float c;         // scale * log2(e)
   unsigned long long wait_limit_ns;
+  // stream-K split of the key range (full attention with a workspace): the flattened
+  // (item, K/V tile) sequence is cut into gridDim.x equal contiguous ranges
+  int streamk;
+  float* ws_part;  // partial rows: [CTA][slot 2][Q tile 2][128 rows][D + 4] fp32 (O~, m, l, pad)
+  int* ws_cnt;     // per (item, Q tile, row): K/V tiles accounted for; back to 0 after use
 };
 
 // ----------------------------------------------------------------------------- waits
@@ -129,8 +134,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 struct Item {
-  int bh, q0, n_kv;
-  bool has1;  // the second 128-row tile holds at least one valid query row
+  int bh, q0;
+  int j0, n_kv;    // this piece covers K/V tiles [j0, j0 + n_kv) of the item
+  bool has1;       // the second 128-row tile holds at least one valid query row
+  bool partial;    // the piece covers only part of the item's key range
+  int item;        // linear item index
+  int slot;        // partial-row slot of this CTA: 0 = first piece of its range, 1 = last
 };
 
 // The r-th work item of this CTA. Items are ordered by decreasing cost (causal) and
@@ -161,7 +170,66 @@ __device__ __forceinline__ Item decode_item(int t, const Params& p) {
   } else {
     it.n_kv = p.n_kv_all;
   }
+  it.j0 = 0;
+  it.partial = false;
+  it.item = t;
+  it.slot = 0;
   return it;
+}
+
+// Stream-K range boundaries: CTA c owns units [bound(c), bound(c+1)) of the flattened
+// (item, K/V tile) sequence of W units.
+__device__ __forceinline__ long long sk_bound(long long c, long long W, long long G) {
+  return (c * W) / G;
+}
+// the CTA whose range contains unit u
+__device__ __forceinline__ int sk_owner(long long u, long long W, long long G) {
+  long long c = (u * G) / W;
+  while (c + 1 < G && sk_bound(c + 1, W, G) <= u) ++c;
+  return (int)c;
+}
+
+// Per-thread iterator over this CTA's pieces; every role walks the same sequence.
+struct Sched {
+  long long u, u1;  // stream-K: next unit, end of range
+  int r;            // otherwise: round of the item deal
+  bool first;
+};
+
+__device__ __forceinline__ Sched sched_begin(const Params& p) {
+  Sched s;
+  s.r = 0;
+  s.first = true;
+  s.u = s.u1 = 0;
+  if (p.streamk) {
+    const long long W = (long long)p.n_items * p.n_kv_all;
+    s.u = sk_bound(blockIdx.x, W, gridDim.x);
+    s.u1 = sk_bound(blockIdx.x + 1, W, gridDim.x);
+  }
+  return s;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ bool sched_next(Sched& s, Item& it, const Params& p) {
+  if (!CAUSAL && p.streamk) {
+    if (s.u >= s.u1) return false;
+    const long long n = p.n_kv_all;
+    const int t = (int)(s.u / n);
+    const long long e = min(s.u1, (long long)(t + 1) * n);
+    it = decode_item<false>(t, p);
+    it.j0 = (int)(s.u - (long long)t * n);
+    it.n_kv = (int)(e - s.u);
+    it.partial = it.n_kv != p.n_kv_all;
+    it.slot = s.first ? 0 : 1;
+    s.first = false;
+    s.u = e;
+    return true;
+  }
+  const int t = item_of(s.r, p);
+  if (t >= p.n_items) return false;
+  ++s.r;
+  it = decode_item<CAUSAL>(t, p);
+  return true;
 }
 
 // ----------------------------------------------------------------------------- kernel
@@ -170,6 +238,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
   using LY = Layout<D>;
+  constexpr int PART_ROW = D + 4;  // O~[D], m, l, 2 pad: rows stay 16-byte aligned
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -246,9 +315,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++ld;
         return true;
       };
-      for (int r = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++r, p)) {
-        const Item it = decode_item<CAUSAL>(t, p);
-        ok = load_kv(&tmK, it.bh, 0);
+      Sched sch = sched_begin(p);
+      Item it;
+      for (int r = 0; ok && sched_next<CAUSAL>(sch, it, p); ++r) {
+        ok = load_kv(&tmK, it.bh, it.j0 * BN);
         if (!ok) break;
         ok = wait_bar(smem_u32(&bars->q_empty), q_ph ^ 1, abort_flag, lim);
         if (!ok) break;
@@ -265,10 +335,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              it.q0 + BM, it.bh, pol_q);
         }
         q_issued = true;
-        ok = load_kv(&tmV, it.bh, 0);
+        ok = load_kv(&tmV, it.bh, it.j0 * BN);
         for (int j = 1; j < it.n_kv && ok; ++j) {
-          ok = load_kv(&tmK, it.bh, j * BN);
-          if (ok) ok = load_kv(&tmV, it.bh, j * BN);
+          ok = load_kv(&tmK, it.bh, (it.j0 + j) * BN);
+          if (ok) ok = load_kv(&tmV, it.bh, (it.j0 + j) * BN);
         }
       }
       if (!ok) {
@@ -330,8 +400,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
       };
-      for (int r = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++r, p)) {
-        const Item it = decode_item<CAUSAL>(t, p);
+      Sched sch = sched_begin(p);
+      Item it;
+      for (int r = 0; ok && sched_next<CAUSAL>(sch, it, p); ++r) {
         uint32_t sK;
         ok = kv_wait(2 * m, sK) && wait_all(smem_u32(&bars->q_full), q_ph);
         if (!ok) break;
@@ -408,8 +479,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float c = p.c;
     uint32_t s_ph = 0, o_ph = 0;
     bool ok = true;
-    for (int rr = 0, t = item_of(0, p); t < p.n_items && ok; t = item_of(++rr, p)) {
-      const Item it = decode_item<CAUSAL>(t, p);
+    Sched sch = sched_begin(p);
+    Item it;
+    for (int rr = 0; ok && sched_next<CAUSAL>(sch, it, p); ++rr) {
       if (g == 1 && !it.has1) continue;
       const int row = it.q0 + g * BM + r;
       const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, kv_lim) visible
@@ -427,7 +499,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
 
-        const int vis = kv_lim - j * BN;
+        const int vis = kv_lim - (it.j0 + j) * BN;
         const bool full = vis >= BN;
         auto sv = [&](int k) { return __uint_as_float(sr[k >> 5][k & 31]); };
         // raw row max over the visible keys (three-input max, four chains)
@@ -527,33 +599,110 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         o_ph ^= 1;
         tc_fence_after();
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
         const bool valid = row < p.Nq;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
-                        ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+        if (!it.partial) {
+          // O = O~ / l, L = (m + log2 l) ln 2
+          const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
+                          ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t o[32];
-          tmem_ld32(tO + q * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
-          uint32_t w16[16];
-          const uint64_t il2 = f2(inv_l, inv_l);
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+            uint32_t w16[16];
+            const uint64_t il2 = f2(inv_l, inv_l);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float x0, x1;
-            f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), il2), x0, x1);
-            w16[k] = pack2<BF16>(x0, x1);
+            for (int k = 0; k < 16; ++k) {
+              float x0, x1;
+              f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), il2), x0, x1);
+              w16[k] = pack2<BF16>(x0, x1);
+            }
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+            }
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
+          if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+          tc_fence_before();
+        } else {
+          // Part of the key range only: keep the state (m, l, O~) of this piece
+          // ("Flash Attention" page, section "平行化": partial states merge with the
+          // associative operator), then the CTA that brings the item's count of merged
+          // K/V tiles to the total merges every piece of the item.
+          float* prow = p.ws_part + ((((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * BM + r) * PART_ROW;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+            float4* dst = reinterpret_cast<float4*>(prow + q * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              __stcg(dst + v, make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                          __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+          }
+          __stcg(reinterpret_cast<float2*>(prow + D), make_float2(m_run, l_run));
+          tc_fence_before();
+          // one counter per query row: this thread's row merges independently of the
+          // other rows, so no synchronisation inside the warpgroup is needed
+          __threadfence();
+          int* cnt = p.ws_cnt + ((size_t)it.item * 2 + g) * BM + r;
+          const int before = atomicAdd(cnt, it.n_kv);
+          if (before + it.n_kv == p.n_kv_all) {
+            atomicExch(cnt, 0);  // every piece of this row is in: ready for the next call
+            __threadfence();
+            const long long W = (long long)p.n_items * p.n_kv_all;
+            const long long G = gridDim.x;
+            const long long ub = (long long)it.item * p.n_kv_all;
+            const int c0 = sk_owner(ub, W, G), c1 = sk_owner(ub + p.n_kv_all - 1, W, G);
+            auto piece_row = [&](int cc) -> const float* {
+              const int slot = sk_bound(cc, W, G) >= ub ? 0 : 1;
+              return p.ws_part + ((((size_t)cc * 2 + slot) * 2 + g) * BM + r) * PART_ROW;
+            };
+            float m = -INFINITY;
+            for (int cc = c0; cc <= c1; ++cc) m = fmaxf(m, __ldcg(piece_row(cc) + D));
+            float l = 0.f;
+            for (int cc = c0; cc <= c1; ++cc) {
+              const float2 ml = __ldcg(reinterpret_cast<const float2*>(piece_row(cc) + D));
+              l += ml.y * ex2_approx(ml.x - m);
+            }
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
+                            ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+              float acc[32];
+#pragma unroll
+              for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+              for (int cc = c0; cc <= c1; ++cc) {
+                const float* pr = piece_row(cc);
+                const float wgt = ex2_approx(__ldcg(pr + D) - m) * inv_l;
+                const float4* src = reinterpret_cast<const float4*>(pr + q * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  const float4 x = __ldcg(src + v);
+                  acc[4 * v] = fmaf(x.x, wgt, acc[4 * v]);
+                  acc[4 * v + 1] = fmaf(x.y, wgt, acc[4 * v + 1]);
+                  acc[4 * v + 2] = fmaf(x.z, wgt, acc[4 * v + 2]);
+                  acc[4 * v + 3] = fmaf(x.w, wgt, acc[4 * v + 3]);
+                }
+              }
+              if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  dst[v] = make_uint4(pack2<BF16>(acc[8 * v], acc[8 * v + 1]), pack2<BF16>(acc[8 * v + 2], acc[8 * v + 3]),
+                                      pack2<BF16>(acc[8 * v + 4], acc[8 * v + 5]), pack2<BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+              }
+            }
+            if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
           }
         }
-        if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
-        tc_fence_before();
       }
     }
     // exit: the load/MMA warpgroup releases Tensor Memory after this barrier
@@ -651,7 +800,7 @@ int device_info(DeviceInfo** out) {
 
 template <int D, bool BF16, bool CAUSAL>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-           DeviceInfo* di, cudaStream_t st) {
+           DeviceInfo* di, int grid, cudaStream_t st) {
   using LY = Layout<D>;
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
   {
@@ -664,10 +813,107 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
       set = true;
     }
   }
-  const int grid = p.n_items < di->sms ? p.n_items : di->sms;
   kern<<<grid, NUM_THREADS, LY::SMEM_BYTES, st>>>(mq, mk, mv, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Stream-K workspace: partial rows of every CTA, then per-row counters.
+struct WsPlan {
+  long long n_items, n_kv, W;
+  int G;
+  size_t part_bytes, cnt_bytes, total;
+};
+WsPlan ws_plan(long long BH, int Nq, int Nk, int d, int sms) {
+  WsPlan w;
+  w.n_items = ((long long)Nq + 2 * BM - 1) / (2 * BM) * BH;
+  w.n_kv = ((long long)Nk + BN - 1) / BN;
+  w.W = w.n_items * w.n_kv;
+  w.G = (int)(w.W < sms ? w.W : sms);
+  auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  w.part_bytes = align((size_t)w.G * 2 * 2 * BM * (d + 4) * sizeof(float));
+  w.cnt_bytes = align((size_t)w.n_items * 2 * BM * sizeof(int));
+  w.total = w.part_bytes + w.cnt_bytes;
+  return w;
+}
+
+// Host-side argument checks shared by the entry points (no CUDA call).
+int check_args(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+               int Nq, int Nk, int d, float scale, fa_dtype dtype, bool* noop) {
+  *noop = false;
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (!(scale >= 0.f) || !isfinite(scale)) return FA_ERR_SCALE;
+  const long long BH = (long long)B * H;
+  if (BH == 0 || Nq == 0) { *noop = true; return FA_OK; }
+  if (Nk == 0) return FA_ERR_EMPTY_KEYS;
+  if (BH > 0x7fffffffLL) return FA_ERR_SHAPE;
+  const long long n_qblk = ((long long)Nq + 2 * BM - 1) / (2 * BM);
+  if (n_qblk * BH > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (!Q || !K || !V || !O || !L) return FA_ERR_NULL;
+  if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)O) & 15) return FA_ERR_ALIGN;
+  if ((uintptr_t)L & 3) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq,
+        int Nk, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+        size_t workspace_bytes, bool use_ws, void* stream) {
+  bool noop = false;
+  int rc = check_args(Q, K, V, O, L, B, H, Nq, Nk, d, scale, dtype, &noop);
+  if (rc != FA_OK || noop) return rc;
+  const long long BH = (long long)B * H;
+  if (use_ws && workspace && ((uintptr_t)workspace & 255)) return FA_ERR_ALIGN;
+
+  DeviceInfo* di = nullptr;
+  rc = device_info(&di);
+  if (rc != FA_OK) return rc;
+
+  Params p;
+  p.O = O;
+  p.L = L;
+  p.BH = (int)BH;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qblk = (int)(((long long)Nq + 2 * BM - 1) / (2 * BM));
+  p.n_items = (int)(p.n_qblk * BH);
+  p.n_kv_all = (Nk + BN - 1) / BN;
+  p.c = scale * 1.4426950408889634f;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.streamk = 0;
+  p.ws_part = nullptr;
+  p.ws_cnt = nullptr;
+  int grid = p.n_items < di->sms ? p.n_items : di->sms;
+  // Full attention whose items do not fill whole waves of SMs: split the key range
+  // (stream-K) when the caller provides the workspace.
+  if (use_ws && !causal && p.n_items % di->sms != 0) {
+    const WsPlan w = ws_plan(BH, Nq, Nk, d, di->sms);
+    if (!workspace || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+    p.streamk = 1;
+    p.ws_part = reinterpret_cast<float*>(workspace);
+    p.ws_cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(workspace) + w.part_bytes);
+    grid = w.G;
+  }
+
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map(&mq, Q, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mk, K, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mv, V, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch<64, false, false>(mq, mk, mv, p, di, grid, st);
+    case 1: return launch<64, false, true>(mq, mk, mv, p, di, grid, st);
+    case 2: return launch<64, true, false>(mq, mk, mv, p, di, grid, st);
+    case 3: return launch<64, true, true>(mq, mk, mv, p, di, grid, st);
+    case 4: return launch<128, false, false>(mq, mk, mv, p, di, grid, st);
+    case 5: return launch<128, false, true>(mq, mk, mv, p, di, grid, st);
+    case 6: return launch<128, true, false>(mq, mk, mv, p, di, grid, st);
+    default: return launch<128, true, true>(mq, mk, mv, p, di, grid, st);
+  }
 }
 
 }  // namespace
@@ -676,55 +922,24 @@ extern "C" {
 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, fa_dtype dtype, void* stream) {
-  // ---- host-side argument checks (no CUDA call before they pass)
-  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-  if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
-  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
-  if (!(scale >= 0.f) || !isfinite(scale)) return FA_ERR_SCALE;
-  const long long BH = (long long)B * H;
-  if (BH == 0 || Nq == 0) return FA_OK;  // nothing to compute
-  if (Nk == 0) return FA_ERR_EMPTY_KEYS;
-  if (BH > 0x7fffffffLL) return FA_ERR_SHAPE;
-  const long long n_qblk = ((long long)Nq + 2 * BM - 1) / (2 * BM);
-  if (n_qblk * BH > 0x7fffffffLL) return FA_ERR_SHAPE;
-  if (!Q || !K || !V || !O || !L) return FA_ERR_NULL;
-  if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)O) & 15) return FA_ERR_ALIGN;
-  if ((uintptr_t)L & 3) return FA_ERR_ALIGN;
+  return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, nullptr, 0, false, stream);
+}
 
+size_t fa_fwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, int causal) {
+  if (causal || B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
   DeviceInfo* di = nullptr;
-  int rc = device_info(&di);
-  if (rc != FA_OK) return rc;
+  if (device_info(&di) != FA_OK) return 0;
+  const long long BH = (long long)B * H;
+  const long long n_items = ((long long)Nq + 2 * BM - 1) / (2 * BM) * BH;
+  if (n_items % di->sms == 0) return 0;
+  return ws_plan(BH, Nq, Nk, d, di->sms).total;
+}
 
-  const bool bf16 = dtype == FA_BF16;
-  CUtensorMap mq, mk, mv;
-  if ((rc = make_map(&mq, Q, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
-  if ((rc = make_map(&mk, K, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
-  if ((rc = make_map(&mv, V, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
-
-  Params p;
-  p.O = O;
-  p.L = L;
-  p.BH = (int)BH;
-  p.Nq = Nq;
-  p.Nk = Nk;
-  p.n_qblk = (int)n_qblk;
-  p.n_items = (int)(n_qblk * BH);
-  p.n_kv_all = (Nk + BN - 1) / BN;
-  p.c = scale * 1.4426950408889634f;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
-
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
-  switch (key) {
-    case 0: return launch<64, false, false>(mq, mk, mv, p, di, st);
-    case 1: return launch<64, false, true>(mq, mk, mv, p, di, st);
-    case 2: return launch<64, true, false>(mq, mk, mv, p, di, st);
-    case 3: return launch<64, true, true>(mq, mk, mv, p, di, st);
-    case 4: return launch<128, false, false>(mq, mk, mv, p, di, st);
-    case 5: return launch<128, false, true>(mq, mk, mv, p, di, st);
-    case 6: return launch<128, true, false>(mq, mk, mv, p, di, st);
-    default: return launch<128, true, true>(mq, mk, mv, p, di, st);
-  }
+int fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+              int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, workspace, workspace_bytes,
+             true, stream);
 }
 
 int fa_last_status(void) {
@@ -754,6 +969,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_TENSOR_MAP: return "the driver rejected a TMA tensor map";
     case FA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
     case FA_ERR_TIMEOUT: return "a device-side pipeline wait exceeded its time limit";
+    case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_fwd_workspace_bytes()";
     default: return "unknown status code";
   }
 }

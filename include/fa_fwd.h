@@ -18,6 +18,8 @@
 #ifndef FA_FWD_H
 #define FA_FWD_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -38,7 +40,8 @@ enum {
   FA_ERR_CUDA = -8,        /* a CUDA runtime call or the kernel launch failed             */
   FA_ERR_TENSOR_MAP = -9,  /* the driver rejected a TMA tensor map for these arguments    */
   FA_ERR_DEVICE = -10,     /* the current device is not an sm_103 GPU                     */
-  FA_ERR_TIMEOUT = -11     /* device-side: a pipeline wait exceeded its time limit        */
+  FA_ERR_TIMEOUT = -11,    /* device-side: a pipeline wait exceeded its time limit        */
+  FA_ERR_WORKSPACE = -12   /* fa_fwd_ws: workspace missing or too small                   */
 };
 
 /* fa_fwd -- launch the attention forward pass on `stream`.
@@ -68,6 +71,30 @@ enum {
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
            int B, int H, int Nq, int Nk, int d, float scale, int causal,
            fa_dtype dtype, void* stream);
+
+/* fa_fwd_workspace_bytes -- size in bytes of the workspace fa_fwd_ws needs for these
+ * sizes on the CURRENT device (it depends on the device's SM count), or 0 when the call
+ * needs none (causal attention, item counts that fill whole waves of SMs, or invalid
+ * sizes). No device memory is touched.
+ *
+ * fa_fwd_ws -- fa_fwd with a caller-provided device workspace that lets full (non-causal)
+ * attention split the key range of work items across CTAs so that every SM gets the same
+ * number of K/V tiles ("stream-K"): a CTA that covers only part of an item's keys stores
+ * the item rows' partial state (m, l, unnormalised O) in the workspace; the CTA that
+ * completes a row's key range merges the partial states with the associative combine of
+ * the online softmax ("Flash Attention" page, section "平行化") and writes O and L.
+ * Same arguments, layout and results as fa_fwd (up to rounding order), plus:
+ *   workspace       device pointer, 256-byte aligned, at least fa_fwd_workspace_bytes()
+ *                   bytes, ZERO-FILLED before its first use; every completed call leaves
+ *                   it zero-filled again (re-zero it after a call that failed on the
+ *                   device, e.g. FA_ERR_TIMEOUT). NULL is allowed when the size is 0.
+ *   workspace_bytes its size.
+ * Calls that share a workspace must not overlap on the GPU. Returns FA_ERR_WORKSPACE when
+ * the workspace is missing or too small, FA_ERR_ALIGN when it is misaligned. */
+size_t fa_fwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, int causal);
+int fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* L,
+              int B, int H, int Nq, int Nk, int d, float scale, int causal,
+              fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /* fa_last_status -- synchronise the current device, then return the device-side status
  * word of libfa on that device: FA_OK, or the first error a kernel recorded since the

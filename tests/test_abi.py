@@ -79,3 +79,16 @@ def test_selftest_rejects_out_of_range_limit():
     import exact_attention_forward_02_gb300 as fa
     assert fa.fa_selftest_wait_timeout(0) == fa.FA_ERR_SHAPE
     assert fa.fa_selftest_wait_timeout(2_000_000) == fa.FA_ERR_SHAPE
+
+
+def test_workspace_variant_host_checks():
+    """fa_fwd_ws shares fa_fwd's host-side checks; sizes are 0 for invalid or causal calls."""
+    import exact_attention_forward_02_gb300 as fa
+    assert fa.fa_fwd_ws(0, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1, 0, 0, None) == fa.FA_ERR_NULL
+    assert fa.fa_fwd_ws(P, P, P, P, P, 1, 1, 128, 128, 32, 0.125, 0, 1, 0, 0, None) == fa.FA_ERR_HEAD_DIM
+    assert fa.fa_fwd_ws(0, 0, 0, 0, 0, 0, 1, 128, 128, 64, 0.125, 0, 1, 0, 0, None) == fa.FA_OK
+    # a misaligned workspace is rejected before any CUDA call
+    assert fa.fa_fwd_ws(P, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1, P + 16, 1 << 20, None) == fa.FA_ERR_ALIGN
+    assert fa.fa_fwd_workspace_bytes(1, 1, 128, 128, 64, True) == 0
+    assert fa.fa_fwd_workspace_bytes(1, 1, 128, 128, 96, False) == 0
+    assert fa.fa_fwd_workspace_bytes(0, 1, 128, 128, 64, False) == 0
