@@ -25,8 +25,9 @@ STATUS = {
     0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_HEAD_DIM", -3: "FA_ERR_SHAPE",
     -4: "FA_ERR_EMPTY_KEYS", -5: "FA_ERR_SCALE", -6: "FA_ERR_ALIGN", -7: "FA_ERR_DTYPE",
     -8: "FA_ERR_CUDA", -9: "FA_ERR_TENSOR_MAP", -10: "FA_ERR_DEVICE", -11: "FA_ERR_TIMEOUT",
-    -12: "FA_ERR_WORKSPACE",
+    -12: "FA_ERR_WORKSPACE", -13: "FA_ERR_SCRATCH_LIMIT",
 }
+FA_NOALLOC_SCRATCH_BYTES = 48 << 20
 globals().update({v: k for k, v in STATUS.items()})
 
 
@@ -49,6 +50,9 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd_ws.restype = ctypes.c_int
     lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_noalloc.restype = ctypes.c_int
+    lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
     lib.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int] * 6
     lib.fa_last_status.restype = ctypes.c_int
@@ -83,6 +87,12 @@ def fa_fwd_ws(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, workspace, w
     return int(lib.fa_fwd_ws(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
                              float(scale), int(bool(causal)), int(dtype), workspace,
                              int(workspace_bytes), stream))
+
+
+def fa_fwd_noalloc(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream) -> int:
+    """C-ABI call of the allocation-free variant (fixed device scratch, see fa_fwd.h)."""
+    return int(lib.fa_fwd_noalloc(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
+                                  float(scale), int(bool(causal)), int(dtype), stream))
 
 
 def fa_fwd_workspace_bytes(B, H, Nq, Nk, d, causal) -> int:

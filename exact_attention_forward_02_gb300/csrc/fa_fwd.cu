@@ -38,6 +38,10 @@
 // Device-side status word (one per device that loads the library).
 __device__ int g_fa_status;
 
+// Fixed scratch of fa_fwd_noalloc: the stream-K workspace for callers that cannot
+// allocate device memory. Every device that loads the library holds it until exit.
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
 namespace fa {
 
 constexpr int BM = 128;                  // query rows per tile = TMEM lanes
@@ -916,6 +920,24 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   }
 }
 
+// Device address of the fixed scratch, looked up once per device (with that device
+// current): in host code the array's name is only a host-side stand-in.
+void* g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fa_noalloc_scratch) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -940,6 +962,30 @@ int fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* L, in
               size_t workspace_bytes, void* stream) {
   return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, workspace, workspace_bytes,
              true, stream);
+}
+
+int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                   int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype, void* stream) {
+  bool noop = false;
+  int rc = check_args(Q, K, V, O, L, B, H, Nq, Nk, d, scale, dtype, &noop);
+  if (rc != FA_OK || noop) return rc;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != FA_OK) return rc;
+  const long long BH = (long long)B * H;
+  const long long n_items = ((long long)Nq + 2 * BM - 1) / (2 * BM) * BH;
+  if (causal || n_items % di->sms == 0)  // no split of the key range: no scratch needed
+    return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, nullptr, 0, false, stream);
+  const WsPlan w = ws_plan(BH, Nq, Nk, d, di->sms);
+  if (w.total > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch)) != FA_OK) return rc;
+  // the per-row counters must start at zero; the array keeps the previous call's contents
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(reinterpret_cast<uint8_t*>(scratch) + w.part_bytes, 0, w.cnt_bytes, st) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, scratch,
+             (size_t)FA_NOALLOC_SCRATCH_BYTES, true, stream);
 }
 
 int fa_last_status(void) {
@@ -970,6 +1016,8 @@ const char* fa_strerror(int code) {
     case FA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
     case FA_ERR_TIMEOUT: return "a device-side pipeline wait exceeded its time limit";
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_fwd_workspace_bytes()";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "the problem needs more scratch than fa_fwd_noalloc's fixed array (FA_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status code";
   }
 }

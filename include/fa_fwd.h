@@ -41,8 +41,12 @@ enum {
   FA_ERR_TENSOR_MAP = -9,  /* the driver rejected a TMA tensor map for these arguments    */
   FA_ERR_DEVICE = -10,     /* the current device is not an sm_103 GPU                     */
   FA_ERR_TIMEOUT = -11,    /* device-side: a pipeline wait exceeded its time limit        */
-  FA_ERR_WORKSPACE = -12   /* fa_fwd_ws: workspace missing or too small                   */
+  FA_ERR_WORKSPACE = -12,  /* fa_fwd_ws: workspace missing or too small                   */
+  FA_ERR_SCRATCH_LIMIT = -13 /* fa_fwd_noalloc: needs more than FA_NOALLOC_SCRATCH_BYTES   */
 };
+
+/* Size of the fixed device scratch array behind fa_fwd_noalloc (48 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES (48u << 20)
 
 /* fa_fwd -- launch the attention forward pass on `stream`.
  *
@@ -95,6 +99,32 @@ size_t fa_fwd_workspace_bytes(int B, int H, int Nq, int Nk, int d, int causal);
 int fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* L,
               int B, int H, int Nq, int Nk, int d, float scale, int causal,
               fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa_fwd_noalloc -- fa_fwd_ws for callers that cannot allocate device memory.
+ *
+ * The method this library implements has no counterpart for this entry point; it exists
+ * for programs that must not call cudaMalloc from inside a library: hosts that hand the
+ * whole device to their own memory pool at start-up, runtimes with a fixed memory budget
+ * that must not grow, and latency-sensitive paths where an allocation (which may
+ * synchronise the device or fail under memory pressure) is not acceptable.
+ *
+ * Same arguments, results and errors as fa_fwd. Full (non-causal) attention whose work
+ * items do not fill whole waves of SMs is split across CTAs exactly like fa_fwd_ws, with
+ * the workspace taken from one file-scope device array of FA_NOALLOC_SCRATCH_BYTES that
+ * every device which loads the library holds until the process exits. Nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library routine is called.
+ *   - The first call on a device looks up that array's device address (once per device,
+ *     with the device current); make that first call before any stream capture.
+ *   - Each call clears the part of the array that must start at zero (with
+ *     cudaMemsetAsync on `stream`) before its launch.
+ *   - All calls share the array: calls that overlap on the GPU (different streams, or
+ *     different host threads) race and give wrong results; serialise them.
+ *   - Returns FA_ERR_SCRATCH_LIMIT, without launching anything, when the sizes need more
+ *     scratch than the array holds (fa_fwd_workspace_bytes() tells how much they need).
+ * Causal attention and problems that need no split use no scratch at all. */
+int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* L,
+                   int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   fa_dtype dtype, void* stream);
 
 /* fa_last_status -- synchronise the current device, then return the device-side status
  * word of libfa on that device: FA_OK, or the first error a kernel recorded since the

@@ -1,0 +1,95 @@
+"""fa_fwd_noalloc: the entry point for callers that cannot allocate device memory (for
+example, hosts whose own pool owns all of the device memory, or processes with a fixed
+memory budget). It splits full attention across CTAs like fa_fwd_ws, with its workspace
+in a fixed device array inside the library instead of a caller allocation.
+
+Checked through the C ABI against the existing workspace entry point, on two calls in a
+row (the fixed array keeps the previous call's contents), plus the size limit."""
+import ctypes
+
+import pytest
+import torch
+
+import gen
+from tests.fa_testlib import TOL_L, TOL_O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_forward_02_gb300 as fa
+    fa.fa_clear_status()
+    return fa
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _run(fa, w, tensors, entry):
+    qd, kd, vd = tensors
+    dev = qd.device
+    O = torch.full((w.B, w.H, w.Nq, w.d), float("nan"), dtype=qd.dtype, device=dev)
+    L = torch.full((w.B, w.H, w.Nq), float("nan"), dtype=torch.float32, device=dev)
+    dt = fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16
+    args = (qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(), L.data_ptr(),
+            w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt)
+    if entry == "noalloc":
+        rc = fa.fa_fwd_noalloc(*args, _stream())
+    else:
+        nbytes = fa.fa_fwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, w.causal)
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        rc = fa.fa_fwd_ws(*args, ws.data_ptr(), ws.numel(), _stream())
+    assert rc == 0, fa.strerror(rc)
+    torch.cuda.synchronize()
+    assert fa.fa_last_status() == 0
+    return O, L
+
+
+@pytest.mark.parametrize("case", [
+    (2, 40, 512, 640, 128, gen.BF16),   # 160 work items on 152 SMs: split key ranges
+    (1, 2, 1000, 4097, 64, gen.F16),    # 8 items split across many CTAs, ragged key tail
+])
+def test_noalloc_matches_workspace_entry_point_twice(fa, case):
+    B, H, Nq, Nk, d, dt = case
+    w = gen.custom(B, H, Nq, Nk, d, dt, False, 1.0, seed=4000 + Nq)
+    assert 0 < fa.fa_fwd_workspace_bytes(B, H, Nq, Nk, d, False) <= fa.FA_NOALLOC_SCRATCH_BYTES
+    dev = torch.device("cuda:0")
+    tensors = tuple(t.to(dev) for t in gen.make_qkv(w))
+    O_ref, L_ref = _run(fa, w, tensors, "ws")
+    for _ in range(2):  # two calls in a row on the shared fixed scratch
+        O, L = _run(fa, w, tensors, "noalloc")
+        assert torch.isfinite(O).all() and torch.isfinite(L).all()
+        assert (O.double() - O_ref.double()).abs().max().item() <= TOL_O[w.dtype]
+        assert (L.double() - L_ref.double()).abs().max().item() <= TOL_L
+
+
+def test_noalloc_causal_needs_no_scratch(fa):
+    w = gen.custom(1, 3, 700, 700, 128, gen.BF16, True, 1.0, seed=41)
+    dev = torch.device("cuda:0")
+    tensors = tuple(t.to(dev) for t in gen.make_qkv(w))
+    O_ref, L_ref = _run(fa, w, tensors, "ws")
+    O, L = _run(fa, w, tensors, "noalloc")
+    assert (O.double() - O_ref.double()).abs().max().item() <= TOL_O[w.dtype]
+    assert (L.double() - L_ref.double()).abs().max().item() <= TOL_L
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(fa):
+    # 16384 work items: the per-row counters alone outgrow what the fixed array leaves
+    B, H, Nq, Nk, d = 128, 64, 512, 128, 128
+    need = fa.fa_fwd_workspace_bytes(B, H, Nq, Nk, d, False)
+    assert need > fa.FA_NOALLOC_SCRATCH_BYTES
+    dev = torch.device("cuda:0")
+    q = torch.zeros((B, H, Nq, d), dtype=torch.bfloat16, device=dev)
+    kv = torch.zeros((B, H, Nk, d), dtype=torch.bfloat16, device=dev)
+    O = torch.empty_like(q)
+    L = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    rc = fa.fa_fwd_noalloc(q.data_ptr(), kv.data_ptr(), kv.data_ptr(), O.data_ptr(), L.data_ptr(),
+                           B, H, Nq, Nk, d, 0.088, False, fa.FA_BF16, _stream())
+    assert rc == fa.FA_ERR_SCRATCH_LIMIT
+    assert "scratch" in fa.strerror(rc)
+    torch.cuda.synchronize()
+    assert fa.fa_last_status() == 0
