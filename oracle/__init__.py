@@ -60,6 +60,9 @@ def _load():
         lib.fa_oracle_block_state.argtypes = [dp, dp, dp, ctypes.c_int, ctypes.c_int64,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                               ctypes.c_int, dp, dp, dp]
+        lib.fa_oracle_attention_bwd.restype = ctypes.c_int
+        lib.fa_oracle_attention_bwd.argtypes = [dp, dp, dp, dp] + [ctypes.c_int] * 5 + [
+            ctypes.c_double, ctypes.c_int, dp, dp, dp, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -78,7 +81,7 @@ class using_library:
         lib = ctypes.CDLL(self.path)
         for name in ("fa_oracle_hw_threads", "fa_oracle_attention", "fa_oracle_attention_rows",
                      "fa_oracle_probs", "fa_oracle_online_softmax", "fa_oracle_merge",
-                     "fa_oracle_block_state"):
+                     "fa_oracle_block_state", "fa_oracle_attention_bwd"):
             f, g = getattr(lib, name), getattr(self._saved, name)
             f.restype, f.argtypes = g.restype, g.argtypes
         _lib = lib
@@ -184,3 +187,18 @@ def block_state(q, K, V, i: int, j0: int, j1: int, scale: float, causal: bool):
                                   float(scale), int(bool(causal)), ctypes.byref(m),
                                   ctypes.byref(den), _ptr(out))
     return m.value, den.value, out
+
+
+def attention_bwd(Q, K, V, dO, scale: float, causal: bool, nthreads: int = 0):
+    """(dQ, dK, dV) of the attention forward for the upstream gradient dO (float64)."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    assert K.shape == V.shape == (B, H, Nk, d) and dO.shape == Q.shape
+    dQ = np.empty_like(Q)
+    dK = np.empty_like(K)
+    dV = np.empty_like(V)
+    _load().fa_oracle_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, Nq, Nk, d,
+                                    float(scale), int(bool(causal)), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                    int(nthreads))
+    return dQ, dK, dV

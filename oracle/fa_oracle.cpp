@@ -18,6 +18,8 @@
 //           (safe softmax, 3 passes) and "平行化" (the (m, d) and (m, d, o~) merge).
 //   [HW]    "手写 Flash Attention：从算法原理到高性能实现": section 2.2 "Online Softmax"
 //           (the worked row [2,1,5,3] with block 2).
+//   [CS336-3] the same CS336 page, part 3 "FlashAttention 反向" (the gradient formulas
+//           dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = dS K tau, dK = dS^T Q tau).
 //
 // Pins (what fixes each function other than itself) live in tests/test_oracle_pins.py.
 // Every exported function is pinned; none is "parity unpinned".
@@ -231,6 +233,65 @@ void fa_oracle_block_state(const double* q, const double* K, const double* V, in
     }
     *m_out = m;
     *d_out = den;
+}
+
+// Gradients of the attention forward with respect to Q, K and V for an upstream gradient
+// dO ([CS336-3]; "Flash Attention" page, "Algorithm 4: backward pass" and its derivation).
+// For each (b, h) the probability matrix is materialised one row at a time by the plain
+// definition (attention_row: scores, mask, safe softmax), then, row i:
+//   dP_ij = <dO_i, V_j>
+//   D_i   = sum_j P_ij dP_ij                    (the softmax Jacobian contracted with dP)
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dQ_i  = scale * sum_j dS_ij K_j
+//   dK_j += scale * dS_ij Q_i,   dV_j += P_ij dO_i
+// All arrays float64 and dense: Q, dO, dQ are [B,H,Nq,d]; K, V, dK, dV are [B,H,Nk,d].
+// Parallel over (b, h). Returns the number of threads used.
+int fa_oracle_attention_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                            int B, int H, int Nq, int Nk, int d, double scale, int causal,
+                            double* dQ, double* dK, double* dV, int nthreads) {
+  const int64_t heads = (int64_t)B * H;
+  if (nthreads <= 0) nthreads = fa_oracle_hw_threads();
+  std::vector<std::thread> th;
+  const int nt = (int)std::min<int64_t>(std::max(1, nthreads), std::max<int64_t>(1, heads));
+  for (int t = 0; t < nt; ++t) {
+    th.emplace_back([&, t]() {
+      std::vector<double> prow((size_t)std::max(Nk, 1)), dprow((size_t)std::max(Nk, 1)), o((size_t)d);
+      for (int64_t bh = t; bh < heads; bh += nt) {
+        const double* q = Q + bh * (int64_t)Nq * d;
+        const double* k = K + bh * (int64_t)Nk * d;
+        const double* v = V + bh * (int64_t)Nk * d;
+        const double* go = dO + bh * (int64_t)Nq * d;
+        double* gq = dQ + bh * (int64_t)Nq * d;
+        double* gk = dK + bh * (int64_t)Nk * d;
+        double* gv = dV + bh * (int64_t)Nk * d;
+        for (int64_t x = 0; x < (int64_t)Nk * d; ++x) { gk[x] = 0.0; gv[x] = 0.0; }
+        for (int64_t i = 0; i < Nq; ++i) {
+          double Lr;
+          attention_row(q + i * d, k, v, Nk, d, scale, causal != 0, i, prow.data(), o.data(), &Lr);
+          double Di = 0.0;
+          for (int j = 0; j < Nk; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += go[i * d + c] * v[(int64_t)j * d + c];
+            dprow[(size_t)j] = acc;
+            Di += prow[(size_t)j] * acc;
+          }
+          for (int c = 0; c < d; ++c) gq[i * d + c] = 0.0;
+          for (int j = 0; j < Nk; ++j) {
+            const double pij = prow[(size_t)j];
+            if (pij == 0.0) continue;
+            const double ds = pij * (dprow[(size_t)j] - Di);
+            for (int c = 0; c < d; ++c) {
+              gq[i * d + c] += scale * ds * k[(int64_t)j * d + c];
+              gk[(int64_t)j * d + c] += scale * ds * q[i * d + c];
+              gv[(int64_t)j * d + c] += pij * go[i * d + c];
+            }
+          }
+        }
+      }
+    });
+  }
+  for (auto& x : th) x.join();
+  return nt;
 }
 
 }  // extern "C"

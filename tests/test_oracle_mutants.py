@@ -7,6 +7,7 @@ import tempfile
 import pytest
 
 import oracle
+from tests import test_oracle_bwd_pins as bpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.cpp")
@@ -29,6 +30,14 @@ MUTANTS = [
      "const double wa = (m_a == NEG_INF) ? 0.0 : std::exp(m - m_a);", ["merge_closed", "merge_blocking"]),
     ("block state: causal mask ignored", "if (causal && (int64_t)j > i) v = NEG_INF;",
      "if (false) v = NEG_INF;", ["merge_blocking_causal"]),
+    ("backward: D not subtracted", "const double ds = pij * (dprow[(size_t)j] - Di);",
+     "const double ds = pij * dprow[(size_t)j];", ["bwd_torch", "bwd_closed"]),
+    ("backward: dK without the scale", "gk[(int64_t)j * d + c] += scale * ds * q[i * d + c];",
+     "gk[(int64_t)j * d + c] += ds * q[i * d + c];", ["bwd_torch", "bwd_fd"]),
+    ("backward: dV from dS instead of P", "gv[(int64_t)j * d + c] += pij * go[i * d + c];",
+     "gv[(int64_t)j * d + c] += ds * go[i * d + c];", ["bwd_torch", "bwd_closed"]),
+    ("backward: dQ uses V instead of K", "gq[i * d + c] += scale * ds * k[(int64_t)j * d + c];",
+     "gq[i * d + c] += scale * ds * v[(int64_t)j * d + c];", ["bwd_torch", "bwd_fd"]),
 ]
 
 PINS = {
@@ -47,6 +56,9 @@ PINS = {
     "merge_closed": lambda: pins.test_merge_two_singletons_closed_form(oracle),
     "merge_blocking": lambda: pins.test_merge_any_blocking_any_order_equals_definition(oracle, False),
     "merge_blocking_causal": lambda: pins.test_merge_any_blocking_any_order_equals_definition(oracle, True),
+    "bwd_torch": lambda: bpins.test_bwd_matches_torch_autograd_float64(oracle, (2, 3, 37, 53, 16), False),
+    "bwd_closed": lambda: bpins.test_bwd_closed_forms(oracle),
+    "bwd_fd": lambda: bpins.test_bwd_central_differences(oracle),
 }
 
 
