@@ -333,6 +333,95 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- backward
+def run_bwd(args):
+    """Backward pass (fa_bwd) on the same two workloads: one step = one backward of each.
+    FLOPs: the five products of the backward, 10*B*H*Nq*Nk*d (halved when causal)."""
+    import numpy as np
+    import torch
+
+    import exact_attention_forward_02_gb300 as fa
+    import gen
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    names = tuple(args.workloads.split(",")) if args.workloads else WORKLOADS
+    wl = [gen.WORKLOADS[n] for n in names]
+    bufs = {}
+    for w in wl:
+        q, k, v = (t.to(dev) for t in gen.make_qkv(w))
+        rng = np.random.default_rng([int(w.seed), 3])
+        do = torch.from_numpy(rng.standard_normal((w.B, w.H, w.Nq, w.d))).to(gen.torch_dtype(w.dtype)).to(dev)
+        O = torch.empty_like(q)
+        L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+        dt = fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16
+        rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(),
+                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt, sp)
+        if rc != 0:
+            raise fa.FAError(rc)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        nws = fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        bufs[w.name] = (q, k, v, O, do, L, dq, dk, dv, ws, dt)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launch(w):
+        q, k, v, O, do, L, dq, dk, dv, ws, dt = bufs[w.name]
+        rc = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), do.data_ptr(),
+                       L.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.Nq,
+                       w.Nk, w.d, w.scale, w.causal, dt, ws.data_ptr(), ws.numel(), sp)
+        if rc != 0:
+            raise fa.FAError(rc)
+
+    fa.fa_clear_status()
+    for _ in range(args.warmup):
+        for w in wl:
+            flush.zero_()
+            launch(w)
+    torch.cuda.synchronize(dev)
+    n = args.steps
+    ev = {w.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)] for w in wl}
+    launches0 = fa.fa_num_kernel_launches()
+    for i in range(n):
+        for w in wl:
+            flush.zero_()
+            a, b = ev[w.name][i]
+            a.record(stream)
+            launch(w)
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = fa.fa_num_kernel_launches() - launches0
+    status = fa.fa_last_status()
+    if status != 0:
+        raise fa.FAError(status, "device status")
+    flops = {w.name: 2.5 * w.flops for w in wl}
+    per = {w.name: [a.elapsed_time(b) for a, b in ev[w.name]] for w in wl}
+    step_ms = sum(statistics.fmean(per[w.name]) for w in wl)
+    peak, _, peak_kind = peaks()
+    value = sum(flops.values()) / (step_ms * 1e-3) / 1e12
+    line = {
+        "metric": "attention bwd TFLOPS (dQ, dK, dV; bf16, causal & full)", "value": round(value, 2),
+        "unit": UNIT, "n_gpus": 1, "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "+".join(sorted({w.dtype for w in wl})), "data": "synthetic",
+        "config": {"workload": "+".join(names), "shapes": [w.describe() for w in wl],
+                   "l2": "flushed before every call (256 MiB write, outside the events)",
+                   "flops": "10*B*H*Nq*Nk*d, halved when causal"},
+        "breakdown": {w.name: {"ms": round(statistics.fmean(per[w.name]), 5),
+                               "tflops": round(flops[w.name] / (statistics.fmean(per[w.name]) * 1e-3) / 1e12, 1),
+                               "pct_of_peak": round(100 * flops[w.name] / (statistics.fmean(per[w.name]) * 1e-3) / 1e12 / peak, 1)}
+                      for w in wl},
+        "roofline": {"bound": "tensor", "achieved": round(value, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(value / peak, 4), "peak_source": f"{peak_kind} bf16 dense",
+                     "traffic": None},
+        "gpu_launches": int(launches),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- oracle
 _HEADS = {}
 
@@ -431,6 +520,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workloads", default="",
                     help="comma-separated workload names (default: the two headline workloads)")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward pass (fa_bwd) instead of the forward")
     ap.add_argument("--streamk", action="store_true",
                     help="call fa_fwd_ws with a workspace (stream-K split of full attention)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
@@ -440,6 +531,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.bwd:
+        run_bwd(args)
     else:
         run_ours(args)
 

@@ -53,6 +53,11 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = [vp] * 9 + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
     lib.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int] * 6
     lib.fa_last_status.restype = ctypes.c_int
@@ -98,6 +103,18 @@ def fa_fwd_noalloc(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream)
 def fa_fwd_workspace_bytes(B, H, Nq, Nk, d, causal) -> int:
     return int(lib.fa_fwd_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(d),
                                           int(bool(causal))))
+
+
+def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+           workspace_bytes, stream) -> int:
+    """C-ABI call of the backward pass (raw device addresses and sizes)."""
+    return int(lib.fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, int(B), int(H), int(Nq), int(Nk), int(d),
+                          float(scale), int(bool(causal)), int(dtype), workspace,
+                          int(workspace_bytes), stream))
+
+
+def fa_bwd_workspace_bytes(B, H, Nq, Nk, d) -> int:
+    return int(lib.fa_bwd_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(d)))
 
 
 def fa_last_status() -> int:

@@ -1,0 +1,635 @@
+// fa_bwd.cuh -- attention backward (dQ, dK, dV) for GB300 (sm_103a). Included by fa_fwd.cu.
+//
+// What it computes (CS336 lecture 5 "05_flash_attention.py", part 3, flash_attention_backward;
+// "Flash Attention" page, "Algorithm 4: backward pass" and its derivation): with
+// S = tau Q K^T (masked), P = exp(S - L) recomputed from the forward's logsumexp L,
+//     dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i o O_i),  dS = P o (dP - D),
+//     dQ = tau dS K,  dK = tau dS^T Q.
+// Two kernels, so that every accumulator fits Tensor Memory and nothing is accumulated
+// with atomics:
+//   fa_bwd_dq_kernel  one 128-row query tile per CTA, looping over key tiles: computes
+//                     D (stored for the second kernel) and dQ; TMEM: S | dP | dQ.
+//   fa_bwd_dkv_kernel one 128-key tile per CTA, looping over query tiles: the transposed
+//                     products S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
+//                     dK += dS^T Q; TMEM: S^T | dP^T | dK | dV.
+// Roles per CTA (6 warps): warps 0-3 elementwise work (thread r owns TMEM lane r), warp 4
+// TMA producer, warp 5 MMA issuer (warp-converged, one elected lane issues).
+#pragma once
+
+namespace fa {
+
+constexpr int BW_WARPS = 6;
+constexpr int BW_THREADS = BW_WARPS * 32;
+constexpr int BW_WARP_LOAD = 4;
+constexpr int BW_WARP_MMA = 5;
+constexpr int BW_MAX_SLOTS = 8;
+
+struct BwdParams {
+  const void* O;      // dq kernel: forward output (16-bit), for D
+  const void* dO;     // dq kernel: upstream gradient rows (16-bit), for D
+  const float* L;     // forward logsumexp (natural log), [BH, Nq]
+  float* Dws;         // D = rowsum(dO o O), [BH, Nq] fp32 (written by the dq kernel)
+  void* dQ;           // outputs (16-bit)
+  void* dK;
+  void* dV;
+  int BH, Nq, Nk;
+  int n_qt, n_kt;     // ceil(Nq/128), ceil(Nk/128)
+  int n_items;
+  float c;            // scale * log2(e)
+  float scale;
+  unsigned long long wait_limit_ns;
+};
+
+struct BwdBars {
+  uint64_t a_full, a_empty;            // the CTA's resident tiles (Q+dO, or K+V)
+  uint64_t full[BW_MAX_SLOTS];         // streamed tile pairs
+  uint64_t release[BW_MAX_SLOTS];
+  uint64_t s_full;                      // both score products of the current tile in TMEM
+  uint64_t p_full;                      // 16-bit operands written back to TMEM
+  uint64_t done;                        // accumulators final for the current item
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+struct BwdLayout {
+  static constexpr int TILE_BYTES = BM * D * 2;
+  static constexpr int CHUNK_BYTES = BM * 128;
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int PAIR_BYTES = 2 * TILE_BYTES;   // a streamed pair of tiles
+  static constexpr int FIXED = 2 * TILE_BYTES + 1024 + 1024;
+  static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / PAIR_BYTES;
+  static constexpr int SLOTS = SLOTS_FIT > BW_MAX_SLOTS ? BW_MAX_SLOTS : SLOTS_FIT;
+  static constexpr int OFF_A = 0;                     // resident pair
+  static constexpr int OFF_S = 2 * TILE_BYTES;        // streamed pairs
+  static constexpr int OFF_LD = OFF_S + SLOTS * PAIR_BYTES;  // 2 x 128 floats (L, D of a tile)
+  static constexpr int OFF_BAR = OFF_LD + 1024;
+  static constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(BwdBars) + 1024;
+  static_assert(SLOTS >= 2, "need two streamed slots");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+};
+
+__device__ __forceinline__ void store_row16(void* base, size_t row, int d_cols, int q32,
+                                            const uint32_t (&w16)[16]) {
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(base) + row * d_cols * 2 + q32 * 64);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+}
+
+// ============================================================================ dQ kernel
+// CTA item: (bh, query tile qt). Streams K_j, V_j; per key tile:
+//   S = Q K_j^T, dP = dO V_j^T  (TMEM)  ->  dS = P o (dP - D)  (16-bit, over S)  ->  dQ += dS K_j
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const BwdParams p) {
+  using LY = BwdLayout<D>;
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_COLS = 512;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + LY::OFF_BAR);
+  const uint32_t sA = smem_u32(smem + LY::OFF_A);   // Q tile, then dO tile
+  const uint32_t sS = smem_u32(smem + LY::OFF_S);   // K_j, V_j pairs
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_kv_all = p.n_kt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->a_full), 1);
+    mbar_init(smem_u32(&bars->a_empty), 1);
+    for (int s = 0; s < LY::SLOTS; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->release[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->p_full), 4);
+    mbar_init(smem_u32(&bars->done), 1);
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BW_WARP_MMA) {
+    tmem_alloc(smem_u32(&bars->tmem_base), T_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const unsigned long long lim = p.wait_limit_ns;
+
+  auto item_tiles = [&](int t, int& bh, int& q0, int& n_kv) {
+    bh = t / p.n_qt;
+    q0 = (t % p.n_qt) * BM;
+    n_kv = CAUSAL ? min(n_kv_all, (min(q0 + BM, p.Nq) - 1) / BN + 1) : n_kv_all;
+  };
+
+  if (warp == BW_WARP_LOAD) {
+    if (lane == 0) {
+      uint32_t j_glob = 0, a_ph = 0;
+      bool ok = true;
+      uint32_t issued = 0, last_par = 0;
+      bool a_issued = false;
+      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+        int bh, q0, n_kv;
+        item_tiles(t, bh, q0, n_kv);
+        ok = wait_bar(smem_u32(&bars->a_empty), a_ph ^ 1, abort_flag, lim);
+        if (!ok) break;
+        a_ph ^= 1;
+        const uint32_t af = smem_u32(&bars->a_full);
+        mbar_arrive_expect_tx(af, 2 * LY::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < LY::CHUNKS; ++c) {
+          tma_load_3d(sA + c * LY::CHUNK_BYTES, &tmQ, af, c * 64, q0, bh);
+          tma_load_3d(sA + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmdO, af, c * 64, q0, bh);
+        }
+        a_issued = true;
+        for (int j = 0; j < n_kv && ok; ++j, ++j_glob) {
+          const uint32_t slot = j_glob % LY::SLOTS, par = (j_glob / LY::SLOTS) & 1u;
+          if (j_glob >= (uint32_t)LY::SLOTS) {
+            const uint32_t u = j_glob - LY::SLOTS;  // the slot's previous tile pair
+            ok = wait_bar(smem_u32(&bars->release[u % LY::SLOTS]), (u / LY::SLOTS) & 1u, abort_flag, lim);
+            if (!ok) break;
+          }
+          const uint32_t f = smem_u32(&bars->full[slot]);
+          mbar_arrive_expect_tx(f, 2 * LY::TILE_BYTES);
+          const uint32_t dst = sS + slot * LY::PAIR_BYTES;
+#pragma unroll
+          for (int c = 0; c < LY::CHUNKS; ++c) {
+            tma_load_3d(dst + c * LY::CHUNK_BYTES, &tmK, f, c * 64, j * BN, bh);
+            tma_load_3d(dst + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, f, c * 64, j * BN, bh);
+          }
+          issued |= 1u << slot;
+          last_par = (last_par & ~(1u << slot)) | (par << slot);
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < LY::SLOTS; ++s)
+          if (issued & (1u << s)) wait_drain(smem_u32(&bars->full[s]), (last_par >> s) & 1u, lim);
+        if (a_issued) wait_drain(smem_u32(&bars->a_full), a_ph ^ 1, lim);
+      }
+    }
+  } else if (warp == BW_WARP_MMA) {
+    constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BM, BN);  // S, dP: K-major x K-major
+    constexpr uint32_t ID_Q = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BM, D);   // dQ: A in TMEM, K MN-major
+    const uint64_t dA = umma_smem_desc(sA, 16, 1024);
+    const uint64_t dB = umma_smem_desc(sS, 16, 1024);
+    const uint64_t dBmn = umma_smem_desc(sS, LY::CHUNK_BYTES, 1024);
+    uint32_t j_glob = 0, a_ph = 0, p_ph = 0;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t par) {
+      return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+    };
+    // S = Q K^T into T_S, dP = dO V^T into T_DP (K = D per product)
+    auto issue_scores = [&](uint32_t slot) {
+      if (elect_one()) {
+        const uint64_t dk = dB + ((slot * LY::PAIR_BYTES) >> 4);
+        const uint64_t dv = dk + (LY::TILE_BYTES >> 4);
+        const uint64_t ddo = dA + (LY::TILE_BYTES >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + T_S, dA + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + T_DP, ddo + off, dv + off, ID_S, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&bars->s_full));
+      }
+      __syncwarp();
+    };
+    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      int bh, q0, n_kv;
+      item_tiles(t, bh, q0, n_kv);
+      (void)bh; (void)q0;
+      ok = wait_all(smem_u32(&bars->a_full), a_ph) &&
+           wait_all(smem_u32(&bars->full[j_glob % LY::SLOTS]), (j_glob / LY::SLOTS) & 1u);
+      if (!ok) break;
+      a_ph ^= 1;
+      tc_fence_after();
+      issue_scores(j_glob % LY::SLOTS);
+      for (int j = 0; j < n_kv; ++j) {
+        const uint32_t slot = (j_glob + j) % LY::SLOTS;
+        ok = wait_all(smem_u32(&bars->p_full), p_ph);
+        if (!ok) break;
+        p_ph ^= 1;
+        tc_fence_after();
+        // dQ += dS K_j : M=128 queries, N=D, K=128 keys; dS from TMEM, K_j MN-major
+        if (elect_one()) {
+          const uint64_t dk = dBmn + ((slot * LY::PAIR_BYTES) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tmem + T_DQ, tmem + T_S + ks * 8, dk + ((ks * 16 * 128) >> 4), ID_Q,
+                    (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        if (j + 1 < n_kv) {
+          const uint32_t nslot = (j_glob + j + 1) % LY::SLOTS;
+          ok = wait_all(smem_u32(&bars->full[nslot]), ((j_glob + j + 1) / LY::SLOTS) & 1u);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(nslot);
+        } else {
+          if (elect_one()) {
+            umma_commit(smem_u32(&bars->done));
+            umma_commit(smem_u32(&bars->a_empty));
+          }
+          __syncwarp();
+        }
+        if (elect_one()) umma_commit(smem_u32(&bars->release[(j_glob + j) % LY::SLOTS]));
+        __syncwarp();
+      }
+      j_glob += n_kv;
+    }
+    if (elect_one()) umma_commit(smem_u32(&bars->mma_drain));
+    __syncwarp();
+    wait_drain(smem_u32(&bars->mma_drain), 0, lim);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------- elementwise
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP, tQ = tmem + lane_off + T_DQ;
+    uint32_t s_ph = 0, d_ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      int bh, q0, n_kv;
+      item_tiles(t, bh, q0, n_kv);
+      const int row = q0 + r;
+      const bool valid = row < p.Nq;
+      const size_t grow = (size_t)bh * p.Nq + (valid ? row : 0);
+      // D = rowsum(dO o O) in fp32 from the 16-bit rows
+      float Drow = 0.f, L2 = INFINITY;
+      if (valid) {
+        const uint4* o4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.O) + grow * D * 2);
+        const uint4* g4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.dO) + grow * D * 2);
+        float acc2[2] = {0.f, 0.f};
+#pragma unroll 4
+        for (int v = 0; v < D / 8; ++v) {
+          const uint4 a = o4[v], b = g4[v];
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float a0, a1, b0, b1;
+            unpack2<BF16>(aw[e], a0, a1);
+            unpack2<BF16>(bw[e], b0, b1);
+            acc2[e & 1] = fmaf(a0, b0, fmaf(a1, b1, acc2[e & 1]));
+          }
+        }
+        Drow = acc2[0] + acc2[1];
+        p.Dws[grow] = Drow;
+        L2 = p.L[grow] * 1.4426950408889634f;
+      }
+      const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;
+      for (int j = 0; j < n_kv; ++j) {
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), s_ph, abort_flag, lim));
+        if (!ok) break;
+        s_ph ^= 1;
+        tc_fence_after();
+        const int vis = kv_lim - j * BN;
+        // two halves of 64 keys: P = exp2(S c - L log2 e), dS = P (dP - D) -> 16-bit over S
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[2][32], dr[2][32];
+          tmem_ld32(tS + h * 64, sr[0]);
+          tmem_ld32(tS + h * 64 + 32, sr[1]);
+          tmem_ld32(tDP + h * 64, dr[0]);
+          tmem_ld32(tDP + h * 64 + 32, dr[1]);
+          tmem_wait_ld();
+          reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int key0 = h * 64 + 2 * k;
+            const float s0 = __uint_as_float(sr[k >> 4][(2 * k) & 31]);
+            const float s1 = __uint_as_float(sr[k >> 4][(2 * k + 1) & 31]);
+            const float g0 = __uint_as_float(dr[k >> 4][(2 * k) & 31]);
+            const float g1 = __uint_as_float(dr[k >> 4][(2 * k + 1) & 31]);
+            const float p0 = key0 < vis ? ex2_approx(fmaf(s0, p.c, -L2)) : 0.f;
+            const float p1 = key0 + 1 < vis ? ex2_approx(fmaf(s1, p.c, -L2)) : 0.f;
+            pk[k] = pack2<BF16>(p0 * (g0 - Drow), p1 * (g1 - Drow));
+          }
+          tmem_st32(tS + h * 32, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+      }
+      if (!ok) break;
+      // dQ = scale * (dS K) -> 16-bit
+      ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->done), d_ph, abort_flag, lim));
+      if (!ok) break;
+      d_ph ^= 1;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld32(tQ + q * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        uint32_t w16[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]) * p.scale, __uint_as_float(o[2 * k + 1]) * p.scale);
+        if (valid) store_row16(p.dQ, grow, D, q, w16);
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == BW_WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, T_COLS);
+  }
+}
+
+// ============================================================================ dK, dV kernel
+// CTA item: (bh, key tile kt). Streams Q_i, dO_i; per query tile:
+//   S^T = K Q_i^T, dP^T = V dO_i^T  (TMEM)  ->  P^T, dS^T (16-bit, over them)
+//   ->  dV += P^T dO_i,  dK += dS^T Q_i
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(BW_THREADS, 1)
+    fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                      const BwdParams p) {
+  using LY = BwdLayout<D>;
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DK = 256, T_DV = 256 + D, T_COLS = 512;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + LY::OFF_BAR);
+  const uint32_t sA = smem_u32(smem + LY::OFF_A);   // K tile, then V tile
+  const uint32_t sS = smem_u32(smem + LY::OFF_S);   // Q_i, dO_i pairs
+  float* sLD = reinterpret_cast<float*>(smem + LY::OFF_LD);  // [0,128): L log2e, [128,256): D
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->a_full), 1);
+    mbar_init(smem_u32(&bars->a_empty), 1);
+    for (int s = 0; s < LY::SLOTS; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->release[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full), 1);
+    mbar_init(smem_u32(&bars->p_full), 4);
+    mbar_init(smem_u32(&bars->done), 1);
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BW_WARP_MMA) {
+    tmem_alloc(smem_u32(&bars->tmem_base), T_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const unsigned long long lim = p.wait_limit_ns;
+
+  // query tiles [i0, n_qt) meet key tile kt (causal: only tiles with a query >= the tile's first key)
+  auto item_tiles = [&](int t, int& bh, int& k0, int& i0, int& n_q) {
+    bh = t / p.n_kt;
+    k0 = (t % p.n_kt) * BN;
+    i0 = CAUSAL ? k0 / BM : 0;
+    n_q = p.n_qt - i0;
+  };
+
+  if (warp == BW_WARP_LOAD) {
+    if (lane == 0) {
+      uint32_t i_glob = 0, a_ph = 0;
+      bool ok = true;
+      uint32_t issued = 0, last_par = 0;
+      bool a_issued = false;
+      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+        int bh, k0, i0, n_q;
+        item_tiles(t, bh, k0, i0, n_q);
+        ok = wait_bar(smem_u32(&bars->a_empty), a_ph ^ 1, abort_flag, lim);
+        if (!ok) break;
+        a_ph ^= 1;
+        const uint32_t af = smem_u32(&bars->a_full);
+        mbar_arrive_expect_tx(af, 2 * LY::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < LY::CHUNKS; ++c) {
+          tma_load_3d(sA + c * LY::CHUNK_BYTES, &tmK, af, c * 64, k0, bh);
+          tma_load_3d(sA + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, af, c * 64, k0, bh);
+        }
+        a_issued = true;
+        for (int i = 0; i < n_q && ok; ++i, ++i_glob) {
+          const uint32_t slot = i_glob % LY::SLOTS, par = (i_glob / LY::SLOTS) & 1u;
+          if (i_glob >= (uint32_t)LY::SLOTS) {
+            const uint32_t u = i_glob - LY::SLOTS;
+            ok = wait_bar(smem_u32(&bars->release[u % LY::SLOTS]), (u / LY::SLOTS) & 1u, abort_flag, lim);
+            if (!ok) break;
+          }
+          const uint32_t f = smem_u32(&bars->full[slot]);
+          mbar_arrive_expect_tx(f, 2 * LY::TILE_BYTES);
+          const uint32_t dst = sS + slot * LY::PAIR_BYTES;
+#pragma unroll
+          for (int c = 0; c < LY::CHUNKS; ++c) {
+            tma_load_3d(dst + c * LY::CHUNK_BYTES, &tmQ, f, c * 64, (i0 + i) * BM, bh);
+            tma_load_3d(dst + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmdO, f, c * 64, (i0 + i) * BM, bh);
+          }
+          issued |= 1u << slot;
+          last_par = (last_par & ~(1u << slot)) | (par << slot);
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < LY::SLOTS; ++s)
+          if (issued & (1u << s)) wait_drain(smem_u32(&bars->full[s]), (last_par >> s) & 1u, lim);
+        if (a_issued) wait_drain(smem_u32(&bars->a_full), a_ph ^ 1, lim);
+      }
+    }
+  } else if (warp == BW_WARP_MMA) {
+    constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BN, BM);  // S^T, dP^T
+    constexpr uint32_t ID_G = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BN, D);   // dV, dK: B MN-major
+    const uint64_t dA = umma_smem_desc(sA, 16, 1024);
+    const uint64_t dB = umma_smem_desc(sS, 16, 1024);
+    const uint64_t dBmn = umma_smem_desc(sS, LY::CHUNK_BYTES, 1024);
+    uint32_t i_glob = 0, a_ph = 0, p_ph = 0;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t par) {
+      return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+    };
+    auto issue_scores = [&](uint32_t slot) {
+      if (elect_one()) {
+        const uint64_t dq = dB + ((slot * LY::PAIR_BYTES) >> 4);
+        const uint64_t ddo = dq + (LY::TILE_BYTES >> 4);
+        const uint64_t dv = dA + (LY::TILE_BYTES >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + T_S, dA + off, dq + off, ID_S, ks > 0 ? 1u : 0u);   // K Q^T
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + T_DP, dv + off, ddo + off, ID_S, ks > 0 ? 1u : 0u); // V dO^T
+        }
+        umma_commit(smem_u32(&bars->s_full));
+      }
+      __syncwarp();
+    };
+    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      int bh, k0, i0, n_q;
+      item_tiles(t, bh, k0, i0, n_q);
+      (void)bh; (void)k0;
+      ok = wait_all(smem_u32(&bars->a_full), a_ph) &&
+           wait_all(smem_u32(&bars->full[i_glob % LY::SLOTS]), (i_glob / LY::SLOTS) & 1u);
+      if (!ok) break;
+      a_ph ^= 1;
+      tc_fence_after();
+      issue_scores(i_glob % LY::SLOTS);
+      for (int i = 0; i < n_q; ++i) {
+        const uint32_t slot = (i_glob + i) % LY::SLOTS;
+        ok = wait_all(smem_u32(&bars->p_full), p_ph);
+        if (!ok) break;
+        p_ph ^= 1;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dq = dBmn + ((slot * LY::PAIR_BYTES) >> 4);
+          const uint64_t ddo = dq + (LY::TILE_BYTES >> 4);
+#pragma unroll
+          for (int ks = 0; ks < BM / 16; ++ks) {  // dV += P^T dO_i (K = 128 queries)
+            umma_ts(tmem + T_DV, tmem + T_S + ks * 8, ddo + ((ks * 16 * 128) >> 4), ID_G,
+                    (i > 0 || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < BM / 16; ++ks) {  // dK += dS^T Q_i
+            umma_ts(tmem + T_DK, tmem + T_DP + ks * 8, dq + ((ks * 16 * 128) >> 4), ID_G,
+                    (i > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        if (i + 1 < n_q) {
+          const uint32_t nslot = (i_glob + i + 1) % LY::SLOTS;
+          ok = wait_all(smem_u32(&bars->full[nslot]), ((i_glob + i + 1) / LY::SLOTS) & 1u);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(nslot);
+        } else {
+          if (elect_one()) {
+            umma_commit(smem_u32(&bars->done));
+            umma_commit(smem_u32(&bars->a_empty));
+          }
+          __syncwarp();
+        }
+        if (elect_one()) umma_commit(smem_u32(&bars->release[(i_glob + i) % LY::SLOTS]));
+        __syncwarp();
+      }
+      i_glob += n_q;
+    }
+    if (elect_one()) umma_commit(smem_u32(&bars->mma_drain));
+    __syncwarp();
+    wait_drain(smem_u32(&bars->mma_drain), 0, lim);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------- elementwise
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;     // key row of the tile (TMEM lane)
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP;
+    const uint32_t tK = tmem + lane_off + T_DK, tV = tmem + lane_off + T_DV;
+    uint32_t s_ph = 0, d_ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      int bh, k0, i0, n_q;
+      item_tiles(t, bh, k0, i0, n_q);
+      const int key = k0 + r;
+      for (int i = 0; i < n_q; ++i) {
+        const int q0 = (i0 + i) * BM;
+        // this query tile's L log2(e) and D, one value per thread (rows past Nq: L = +inf
+        // so that P = 0); the previous tile's readers finished at the barrier that ended
+        // its iteration
+        {
+          const int qrow = q0 + r;
+          const bool qv = qrow < p.Nq;
+          const size_t g = (size_t)bh * p.Nq + (qv ? qrow : 0);
+          sLD[r] = qv ? p.L[g] * 1.4426950408889634f : INFINITY;
+          sLD[128 + r] = qv ? p.Dws[g] : 0.f;
+        }
+        // one barrier both publishes sLD and makes the wait's outcome the same in all four
+        // warps (so that a timeout ends the loop everywhere, never at a barrier)
+        ok = named_bar_red_and(2, 128, wait_bar(smem_u32(&bars->s_full), s_ph, abort_flag, lim));
+        if (!ok) break;
+        s_ph ^= 1;
+        tc_fence_after();
+        // causal: query q sees this key iff q >= key; first visible query of the tile:
+        const int qfirst = CAUSAL ? key - q0 : 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[2][32], dr[2][32];
+          tmem_ld32(tS + h * 64, sr[0]);
+          tmem_ld32(tS + h * 64 + 32, sr[1]);
+          tmem_ld32(tDP + h * 64, dr[0]);
+          tmem_ld32(tDP + h * 64 + 32, dr[1]);
+          tmem_wait_ld();
+          reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
+          uint32_t pp[32], pd[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int qc = h * 64 + 2 * k;  // query column within the tile
+            const float2 l2 = *reinterpret_cast<const float2*>(sLD + qc);
+            const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + qc);
+            const float s0 = __uint_as_float(sr[k >> 4][(2 * k) & 31]);
+            const float s1 = __uint_as_float(sr[k >> 4][(2 * k + 1) & 31]);
+            const float g0 = __uint_as_float(dr[k >> 4][(2 * k) & 31]);
+            const float g1 = __uint_as_float(dr[k >> 4][(2 * k + 1) & 31]);
+            const float p0 = qc >= qfirst ? ex2_approx(fmaf(s0, p.c, -l2.x)) : 0.f;
+            const float p1 = qc + 1 >= qfirst ? ex2_approx(fmaf(s1, p.c, -l2.y)) : 0.f;
+            pp[k] = pack2<BF16>(p0, p1);
+            pd[k] = pack2<BF16>(p0 * (g0 - dd.x), p1 * (g1 - dd.y));
+          }
+          tmem_st32(tS + h * 32, pp);
+          tmem_st32(tDP + h * 32, pd);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+        named_bar_sync(2, 128);  // every thread is done reading sLD
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->done), d_ph, abort_flag, lim));
+      if (!ok) break;
+      d_ph ^= 1;
+      tc_fence_after();
+      const bool valid = key < p.Nk;
+      const size_t grow = (size_t)bh * p.Nk + (valid ? key : 0);
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        uint32_t w16[16];
+        tmem_ld32(tK + q * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]) * p.scale, __uint_as_float(o[2 * k + 1]) * p.scale);
+        if (valid) store_row16(p.dK, grow, D, q, w16);
+        tmem_ld32(tV + q * 32, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1]));
+        if (valid) store_row16(p.dV, grow, D, q, w16);
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == BW_WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, T_COLS);
+  }
+}
+
+}  // namespace fa

@@ -731,6 +731,8 @@ __global__ void fa_wait_selftest_kernel(unsigned long long limit_ns) {
 
 }  // namespace fa
 
+#include "fa_bwd.cuh"
+
 // ============================================================================= host side
 namespace {
 
@@ -920,6 +922,42 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   }
 }
 
+// ---------------------------------------------------------------------------- backward
+template <int D, bool BF16, bool CAUSAL>
+int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+               const CUtensorMap& mdo, BwdParams p, DeviceInfo* di, cudaStream_t st) {
+  using LY = BwdLayout<D>;
+  auto kq = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
+  auto kkv = fa_bwd_dkv_kernel<D, BF16, CAUSAL>;
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  // query tiles first: D (needed by the second kernel) and dQ
+  p.n_items = p.BH * p.n_qt;
+  int grid = p.n_items < di->sms ? p.n_items : di->sms;
+  kq<<<grid, BW_THREADS, LY::SMEM_BYTES, st>>>(mq, mdo, mk, mv, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
+  p.n_items = p.BH * p.n_kt;
+  grid = p.n_items < di->sms ? p.n_items : di->sms;
+  kkv<<<grid, BW_THREADS, LY::SMEM_BYTES, st>>>(mk, mv, mq, mdo, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t bwd_ws_bytes(long long BH, int Nq) {
+  return (((size_t)BH * (size_t)Nq * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 // Device address of the fixed scratch, looked up once per device (with that device
 // current): in host code the array's name is only a host-side stand-in.
 void* g_noalloc_addr[kMaxDevices] = {};
@@ -986,6 +1024,66 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
     return FA_ERR_CUDA;
   return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, scratch,
              (size_t)FA_NOALLOC_SCRATCH_BYTES, true, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+  return bwd_ws_bytes((long long)B * H, Nq);
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+           const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
+           float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+           void* stream) {
+  bool noop = false;
+  // Q, K, V as in the forward; O stands in for the output argument of the shared checks
+  int rc = check_args(Q, K, V, const_cast<void*>(O), const_cast<float*>(L), B, H, Nq, Nk, d, scale,
+                      dtype, &noop);
+  if (rc != FA_OK) return rc;
+  if (noop) return FA_OK;
+  if (!dO || !dQ || !dK || !dV) return FA_ERR_NULL;
+  if (((uintptr_t)dO | (uintptr_t)dQ | (uintptr_t)dK | (uintptr_t)dV) & 15) return FA_ERR_ALIGN;
+  const long long BH = (long long)B * H;
+  if (!workspace || workspace_bytes < bwd_ws_bytes(BH, Nq)) return FA_ERR_WORKSPACE;
+  if ((uintptr_t)workspace & 15) return FA_ERR_ALIGN;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != FA_OK) return rc;
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap mq, mk, mv, mdo;
+  if ((rc = make_map(&mq, Q, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mk, K, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mv, V, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mdo, dO, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
+  BwdParams p;
+  p.O = O;
+  p.dO = dO;
+  p.L = L;
+  p.Dws = reinterpret_cast<float*>(workspace);
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.BH = (int)BH;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qt = (Nq + BM - 1) / BM;
+  p.n_kt = (Nk + BN - 1) / BN;
+  p.n_items = 0;
+  p.c = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  if ((long long)p.n_qt * BH > 0x7fffffffLL || (long long)p.n_kt * BH > 0x7fffffffLL) return FA_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch_bwd<64, false, false>(mq, mk, mv, mdo, p, di, st);
+    case 1: return launch_bwd<64, false, true>(mq, mk, mv, mdo, p, di, st);
+    case 2: return launch_bwd<64, true, false>(mq, mk, mv, mdo, p, di, st);
+    case 3: return launch_bwd<64, true, true>(mq, mk, mv, mdo, p, di, st);
+    case 4: return launch_bwd<128, false, false>(mq, mk, mv, mdo, p, di, st);
+    case 5: return launch_bwd<128, false, true>(mq, mk, mv, mdo, p, di, st);
+    case 6: return launch_bwd<128, true, false>(mq, mk, mv, mdo, p, di, st);
+    default: return launch_bwd<128, true, true>(mq, mk, mv, mdo, p, di, st);
+  }
 }
 
 int fa_last_status(void) {

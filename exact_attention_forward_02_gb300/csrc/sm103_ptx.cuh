@@ -223,6 +223,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// named barrier that also ANDs a predicate over its `count` threads
+__device__ __forceinline__ bool named_bar_red_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %3, 0;\n\t"
+      "bar.red.and.pred po, %1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"(id), "r"(count), "r"((uint32_t)pred)
+      : "memory");
+  return out != 0;
+}
+
 // ----------------------------------------------------------------------------- registers
 // Per-warpgroup register budget changes; every warp of the warpgroup executes the same one.
 template <uint32_t N>
@@ -280,6 +294,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   }
   return r;
+}
+
+// unpack one 32-bit word of two 16-bit values (low half first) into fp32
+template <bool BF16>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+  if constexpr (BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  } else {
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+  }
 }
 
 }  // namespace fa

@@ -126,6 +126,27 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    fa_dtype dtype, void* stream);
 
+/* fa_bwd -- gradients of the forward pass: dQ, dK, dV for the upstream gradient dO
+ * (CS336 lecture 5 "05_flash_attention.py", part 3, flash_attention_backward; "Flash
+ * Attention" page, "Algorithm 4: backward pass"): with S = scale Q K^T (masked as in the
+ * forward) and P = exp(S - L) recomputed from the forward's logsumexp L,
+ *     dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i o O_i),  dS = P o (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ * Arguments (DEVICE pointers, dense row-major, 16-byte aligned, element type `dtype`):
+ *   Q, O, dO, dQ  [B, H, Nq, d];  K, V, dK, dV  [B, H, Nk, d]
+ *   L             [B, H, Nq] fp32, the natural-log logsumexp fa_fwd wrote with O
+ *   workspace     at least fa_bwd_workspace_bytes() bytes, 16-byte aligned, no
+ *                 initialisation needed (it receives D, one fp32 per query row)
+ * d, scale, causal, dtype and stream as in fa_fwd. Two kernels are queued on `stream`
+ * (query tiles: D and dQ; then key tiles: dK and dV); nothing is accumulated with atomics.
+ * dS is rounded to the input type before the products that use it, P before dV.
+ * Errors as fa_fwd, plus FA_ERR_WORKSPACE for a missing or small workspace. */
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+           const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
+           float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+           void* stream);
+
 /* fa_last_status -- synchronise the current device, then return the device-side status
  * word of libfa on that device: FA_OK, or the first error a kernel recorded since the
  * last fa_clear_status() (FA_ERR_TIMEOUT when a bounded pipeline wait gave up; the kernel

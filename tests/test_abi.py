@@ -92,3 +92,16 @@ def test_workspace_variant_host_checks():
     assert fa.fa_fwd_workspace_bytes(1, 1, 128, 128, 64, True) == 0
     assert fa.fa_fwd_workspace_bytes(1, 1, 128, 128, 96, False) == 0
     assert fa.fa_fwd_workspace_bytes(0, 1, 128, 128, 64, False) == 0
+
+
+def test_backward_host_checks():
+    import exact_attention_forward_02_gb300 as fa
+    base = (P, P, P, P, P, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1)
+    assert fa.fa_bwd(0, *base[1:], P, 1 << 20, None) == fa.FA_ERR_NULL
+    assert fa.fa_bwd(*base[:4], 0, *base[5:], P, 1 << 20, None) == fa.FA_ERR_NULL      # dO
+    assert fa.fa_bwd(*base[:6], P + 2, *base[7:], P, 1 << 20, None) == fa.FA_ERR_ALIGN  # dQ
+    assert fa.fa_bwd(*base[:13], 96, *base[14:], P, 1 << 20, None) == fa.FA_ERR_HEAD_DIM
+    assert fa.fa_bwd(*base, 0, 0, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd(*base, P + 4, 1 << 20, None) == fa.FA_ERR_ALIGN
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 50, 64) == 2 * 3 * 100 * 4 + (256 - (2 * 3 * 100 * 4) % 256) % 256
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 50, 96) == 0
