@@ -70,6 +70,13 @@ struct BwdLayout {
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
 
+// the r-th item of this CTA: boustrophedon deal (b, 2G-1-b, 2G+b, ...) of items sorted
+// by decreasing cost
+__device__ __forceinline__ int bw_item_of(int r) {
+  const int G = gridDim.x, b = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - b) : b);
+}
+
 __device__ __forceinline__ void store_row16(void* base, size_t row, int d_cols, int q32,
                                             const uint32_t (&w16)[16]) {
   uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(base) + row * d_cols * 2 + q32 * 64);
@@ -120,9 +127,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const uint32_t tmem = bars->tmem_base;
   const unsigned long long lim = p.wait_limit_ns;
 
+  // causal: heaviest (last) query tiles first; full: head by head (K/V reuse in L2)
   auto item_tiles = [&](int t, int& bh, int& q0, int& n_kv) {
-    bh = t / p.n_qt;
-    q0 = (t % p.n_qt) * BM;
+    if (CAUSAL) {
+      bh = t % p.BH;
+      q0 = (p.n_qt - 1 - t / p.BH) * BM;
+    } else {
+      bh = t / p.n_qt;
+      q0 = (t % p.n_qt) * BM;
+    }
     n_kv = CAUSAL ? min(n_kv_all, (min(q0 + BM, p.Nq) - 1) / BN + 1) : n_kv_all;
   };
 
@@ -132,7 +145,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       bool ok = true;
       uint32_t issued = 0, last_par = 0;
       bool a_issued = false;
-      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
         int bh, q0, n_kv;
         item_tiles(t, bh, q0, n_kv);
         ok = wait_bar(smem_u32(&bars->a_empty), a_ph ^ 1, abort_flag, lim);
@@ -202,7 +215,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       }
       __syncwarp();
     };
-    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+    for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, q0, n_kv;
       item_tiles(t, bh, q0, n_kv);
       (void)bh; (void)q0;
@@ -257,7 +270,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP, tQ = tmem + lane_off + T_DQ;
     uint32_t s_ph = 0, d_ph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+    for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, q0, n_kv;
       item_tiles(t, bh, q0, n_kv);
       const int row = q0 + r;
@@ -395,9 +408,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const unsigned long long lim = p.wait_limit_ns;
 
   // query tiles [i0, n_qt) meet key tile kt (causal: only tiles with a query >= the tile's first key)
+  // causal: heaviest (first) key tiles first; full: head by head (Q/dO reuse in L2)
   auto item_tiles = [&](int t, int& bh, int& k0, int& i0, int& n_q) {
-    bh = t / p.n_kt;
-    k0 = (t % p.n_kt) * BN;
+    if (CAUSAL) {
+      bh = t % p.BH;
+      k0 = (t / p.BH) * BN;
+    } else {
+      bh = t / p.n_kt;
+      k0 = (t % p.n_kt) * BN;
+    }
     i0 = CAUSAL ? k0 / BM : 0;
     n_q = p.n_qt - i0;
   };
@@ -408,7 +427,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       bool ok = true;
       uint32_t issued = 0, last_par = 0;
       bool a_issued = false;
-      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
         int bh, k0, i0, n_q;
         item_tiles(t, bh, k0, i0, n_q);
         ok = wait_bar(smem_u32(&bars->a_empty), a_ph ^ 1, abort_flag, lim);
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       }
       __syncwarp();
     };
-    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+    for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, k0, i0, n_q;
       item_tiles(t, bh, k0, i0, n_q);
       (void)bh; (void)k0;
@@ -539,7 +558,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t tK = tmem + lane_off + T_DK, tV = tmem + lane_off + T_DV;
     uint32_t s_ph = 0, d_ph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+    for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, k0, i0, n_q;
       item_tiles(t, bh, k0, i0, n_q);
       const int key = k0 + r;
