@@ -63,8 +63,41 @@ def _load():
         lib.fa_oracle_attention_bwd.restype = ctypes.c_int
         lib.fa_oracle_attention_bwd.argtypes = [dp, dp, dp, dp] + [ctypes.c_int] * 5 + [
             ctypes.c_double, ctypes.c_int, dp, dp, dp, ctypes.c_int]
+        _declare_dropout(lib)
         _lib = lib
     return _lib
+
+
+def _declare_dropout(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    u64, u32 = ctypes.c_uint64, ctypes.c_uint32
+    lib.fa_oracle_philox4x32_10.restype = None
+    lib.fa_oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+    lib.fa_oracle_dropout_threshold.restype = ctypes.c_int
+    lib.fa_oracle_dropout_threshold.argtypes = [ctypes.c_double]
+    lib.fa_oracle_dropout_keep.restype = ctypes.c_int
+    lib.fa_oracle_dropout_keep.argtypes = [ctypes.c_int] * 4 + [ctypes.c_double, u64, u32,
+                                                                ctypes.POINTER(ctypes.c_uint8)]
+    lib.fa_oracle_attention_dropout.restype = ctypes.c_int
+    lib.fa_oracle_attention_dropout.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_int, ctypes.c_double, u64, u32, dp, dp, ctypes.c_int]
+    lib.fa_oracle_attention_dropout_rows.restype = ctypes.c_int
+    lib.fa_oracle_attention_dropout_rows.argtypes = [dp, dp, dp] + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_int, ctypes.c_double, u64, u32, i64p, ctypes.c_int64, dp, dp,
+        ctypes.c_int]
+    lib.fa_oracle_attention_bwd_dropout.restype = ctypes.c_int
+    lib.fa_oracle_attention_bwd_dropout.argtypes = [dp, dp, dp, dp] + [ctypes.c_int] * 5 + [
+        ctypes.c_double, ctypes.c_int, ctypes.c_double, u64, u32, dp, dp, dp, ctypes.c_int]
+
+
+_EXPORTS = ("fa_oracle_hw_threads", "fa_oracle_attention", "fa_oracle_attention_rows",
+            "fa_oracle_probs", "fa_oracle_online_softmax", "fa_oracle_merge",
+            "fa_oracle_block_state", "fa_oracle_attention_bwd", "fa_oracle_philox4x32_10",
+            "fa_oracle_dropout_threshold", "fa_oracle_dropout_keep",
+            "fa_oracle_attention_dropout", "fa_oracle_attention_dropout_rows",
+            "fa_oracle_attention_bwd_dropout")
 
 
 class using_library:
@@ -79,9 +112,7 @@ class using_library:
         _load()
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
-        for name in ("fa_oracle_hw_threads", "fa_oracle_attention", "fa_oracle_attention_rows",
-                     "fa_oracle_probs", "fa_oracle_online_softmax", "fa_oracle_merge",
-                     "fa_oracle_block_state", "fa_oracle_attention_bwd"):
+        for name in _EXPORTS:
             f, g = getattr(lib, name), getattr(self._saved, name)
             f.restype, f.argtypes = g.restype, g.argtypes
         _lib = lib
@@ -201,4 +232,88 @@ def attention_bwd(Q, K, V, dO, scale: float, causal: bool, nthreads: int = 0):
     _load().fa_oracle_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, Nq, Nk, d,
                                     float(scale), int(bool(causal)), _ptr(dQ), _ptr(dK), _ptr(dV),
                                     int(nthreads))
+    return dQ, dK, dV
+
+
+def philox4x32_10(ctr, key):
+    """The four 32-bit output words of Philox-4x32-10 for one counter and key."""
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    assert c.shape == (4,) and k.shape == (2,)
+    out = np.zeros(4, np.uint32)
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    _load().fa_oracle_philox4x32_10(c.ctypes.data_as(u32p), k.ctypes.data_as(u32p),
+                                    out.ctypes.data_as(u32p))
+    return out
+
+
+def dropout_threshold(p_drop: float) -> int:
+    """The 15-bit threshold t of p_drop, or -1 when p_drop is out of range."""
+    return int(_load().fa_oracle_dropout_threshold(float(p_drop)))
+
+
+def dropout_keep(B: int, H: int, Nq: int, Nk: int, p_drop: float, seed: int, offset: int):
+    """The keep mask [B,H,Nq,Nk] (uint8, 1 = kept) of the dropout definition."""
+    keep = np.zeros((B, H, Nq, Nk), np.uint8)
+    rc = _load().fa_oracle_dropout_keep(int(B), int(H), int(Nq), int(Nk), float(p_drop),
+                                        int(seed), int(offset),
+                                        keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    if rc != 0:
+        raise ValueError(f"invalid dropout probability {p_drop}")
+    return keep
+
+
+def attention_dropout(Q, K, V, scale: float, causal: bool, p_drop: float, seed: int,
+                      offset: int, nthreads: int = 0):
+    """O [B,H,Nq,d], L [B,H,Nq] of attention with dropout (the mask of seed/offset)."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    assert K.shape == (B, H, Nk, d) and V.shape == (B, H, Nk, d)
+    O = np.empty((B, H, Nq, d), np.float64)
+    L = np.empty((B, H, Nq), np.float64)
+    rc = _load().fa_oracle_attention_dropout(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d,
+                                             float(scale), int(bool(causal)), float(p_drop),
+                                             int(seed), int(offset), _ptr(O), _ptr(L),
+                                             int(nthreads))
+    if rc < 0:
+        raise ValueError(f"invalid dropout probability {p_drop}")
+    return O, L
+
+
+def attention_dropout_rows(Q, K, V, scale: float, causal: bool, p_drop: float, seed: int,
+                           offset: int, rows, nthreads: int = 0):
+    """attention_dropout on selected flat rows r = (b*H + h)*Nq + i: O [n,d], L [n]."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert rows.ndim == 1 and (rows.size == 0 or (rows.min() >= 0 and rows.max() < B * H * Nq))
+    n = rows.size
+    O = np.empty((n, d), np.float64)
+    L = np.empty((n,), np.float64)
+    rc = _load().fa_oracle_attention_dropout_rows(
+        _ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+        float(p_drop), int(seed), int(offset),
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(O), _ptr(L), int(nthreads))
+    if rc < 0:
+        raise ValueError(f"invalid dropout probability {p_drop}")
+    return O, L
+
+
+def attention_bwd_dropout(Q, K, V, dO, scale: float, causal: bool, p_drop: float, seed: int,
+                          offset: int, nthreads: int = 0):
+    """(dQ, dK, dV) of the dropout forward (mask of seed/offset) for upstream gradient dO."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    assert K.shape == V.shape == (B, H, Nk, d) and dO.shape == Q.shape
+    dQ = np.empty_like(Q)
+    dK = np.empty_like(K)
+    dV = np.empty_like(V)
+    rc = _load().fa_oracle_attention_bwd_dropout(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+        float(p_drop), int(seed), int(offset), _ptr(dQ), _ptr(dK), _ptr(dV), int(nthreads))
+    if rc < 0:
+        raise ValueError(f"invalid dropout probability {p_drop}")
     return dQ, dK, dV

@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_bwd_pins as bpins
+from tests import test_oracle_dropout_pins as dpins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.cpp")
@@ -34,10 +35,28 @@ MUTANTS = [
      "const double ds = pij * dprow[(size_t)j];", ["bwd_torch", "bwd_closed"]),
     ("backward: dK without the scale", "gk[(int64_t)j * d + c] += scale * ds * q[i * d + c];",
      "gk[(int64_t)j * d + c] += ds * q[i * d + c];", ["bwd_torch", "bwd_fd"]),
-    ("backward: dV from dS instead of P", "gv[(int64_t)j * d + c] += pij * go[i * d + c];",
+    ("backward: dV from dS instead of P", "gv[(int64_t)j * d + c] += pz * go[i * d + c];",
      "gv[(int64_t)j * d + c] += ds * go[i * d + c];", ["bwd_torch", "bwd_closed"]),
     ("backward: dQ uses V instead of K", "gq[i * d + c] += scale * ds * k[(int64_t)j * d + c];",
      "gq[i * d + c] += scale * ds * v[(int64_t)j * d + c];", ["bwd_torch", "bwd_fd"]),
+    ("philox: multipliers swapped", "const uint64_t p0 = (uint64_t)0xD2511F53u * c0;",
+     "const uint64_t p0 = (uint64_t)0xCD9E8D57u * c0;", ["philox_kat"]),
+    ("philox: second key word not bumped", "k1 += 0xBB67AE85u;", "k1 += 0u;", ["philox_kat"]),
+    ("dropout: keep only above the threshold", "return x >= dr.t;", "return x > dr.t;",
+     ["dropout_kat_bits"]),
+    ("dropout: halves of a word swapped", "((j & 1) ? (word >> 16) : word)",
+     "((j & 1) ? word : (word >> 16))", ["dropout_kat_bits"]),
+    ("dropout: row and head swapped in the counter",
+     "{(uint32_t)(j >> 3), (uint32_t)i, (uint32_t)bh, dr.offset}",
+     "{(uint32_t)(j >> 3), (uint32_t)bh, (uint32_t)i, dr.offset}", ["dropout_layout"]),
+    ("dropout: threshold truncated", "std::floor(p * 32768.0 + 0.5)", "std::floor(p * 32768.0)",
+     ["dropout_threshold"]),
+    ("dropout: kept entries not rescaled", "dr.z_keep = 32768.0 / (32768.0 - (double)t);",
+     "dr.z_keep = 1.0;", ["dropout_unbiased", "dropout_onehot"]),
+    ("dropout backward: dP without the mask", "dprow[(size_t)j] = acc * zrow[(size_t)j];",
+     "dprow[(size_t)j] = acc;", ["dropout_torch", "dropout_fd"]),
+    ("dropout backward: dV without the mask", "gv[(int64_t)j * d + c] += pz * go[i * d + c];",
+     "gv[(int64_t)j * d + c] += pij * go[i * d + c];", ["dropout_torch", "dropout_fd"]),
 ]
 
 PINS = {
@@ -59,6 +78,14 @@ PINS = {
     "bwd_torch": lambda: bpins.test_bwd_matches_torch_autograd_float64(oracle, (2, 3, 37, 53, 16), False),
     "bwd_closed": lambda: bpins.test_bwd_closed_forms(oracle),
     "bwd_fd": lambda: bpins.test_bwd_central_differences(oracle),
+    "philox_kat": lambda: dpins.test_philox_known_answer_vectors(oracle),
+    "dropout_kat_bits": lambda: dpins.test_mask_bits_from_the_first_known_answer_vector(oracle),
+    "dropout_layout": lambda: dpins.test_philox_matches_triton_and_mask_layout(oracle),
+    "dropout_threshold": lambda: dpins.test_threshold_rounding_and_range(oracle),
+    "dropout_unbiased": lambda: dpins.test_dropout_is_unbiased_over_seeds(oracle),
+    "dropout_onehot": lambda: dpins.test_one_hot_values_read_the_mask_out_of_the_output(oracle),
+    "dropout_torch": lambda: dpins.test_dropout_forward_and_backward_match_torch_autograd(oracle, True),
+    "dropout_fd": lambda: dpins.test_dropout_backward_central_differences(oracle),
 }
 
 
