@@ -200,10 +200,18 @@ def run_ours(args):
         devbuf[w.name] = (qd, kd, vd, O, L, wsp)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    drop_offset = [0]
+
     def launch(w):
         qd, kd, vd, O, L, wsp = devbuf[w.name]
         dt = fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16
-        if wsp is None:
+        if args.dropout > 0:
+            # a fresh mask per call: the offset advances like a training loop's would
+            drop_offset[0] += 1
+            rc = fa.fa_fwd_dropout(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(),
+                                   L.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt,
+                                   args.dropout, 1234, drop_offset[0], sp)
+        elif wsp is None:
             rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(), L.data_ptr(),
                            w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt, sp)
         else:
@@ -310,15 +318,18 @@ def run_ours(args):
                        "shapes": [w.describe() for w in wl],
                        "l2": "flushed before every launch (256 MiB write, outside the events)",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
-                       "entry_point": "fa_fwd_ws (stream-K)" if args.streamk else "fa_fwd",
+                       "entry_point": ("fa_fwd_dropout" if args.dropout > 0 else
+                                       "fa_fwd_ws (stream-K)" if args.streamk else "fa_fwd"),
+                       "dropout": args.dropout,
                        "pct_of_peak": round(100 * value / ws / peak, 1)},
             "breakdown": breakdown,
             "roofline": {"bound": "tensor",
-                         "kernel": f"fa_fwd_kernel<{wd.d}, {wd.dtype}, {'causal' if wd.causal else 'full'}> on {dominant}",
+                         "kernel": f"fa_fwd_kernel<{wd.d}, {wd.dtype}, {'causal' if wd.causal else 'full'}"
+                                   f"{', dropout' if args.dropout > 0 else ''}> on {dominant}",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} bf16 dense (burst: kernel timed alone)",
-                         "traffic": recorded_traffic(dominant),
+                         "traffic": recorded_traffic(dominant) if args.dropout == 0 else None,
                          "algorithmic_bytes": wd.io_bytes},
             "clocks": clk,
             "e2e": {"value": round(whole_job_tflops(flops_step, ws, e2e_ms_max), 2), "unit": UNIT,
@@ -522,6 +533,8 @@ def main():
                     help="comma-separated workload names (default: the two headline workloads)")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass (fa_bwd) instead of the forward")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="time fa_fwd_dropout with this dropout probability (default: no dropout)")
     ap.add_argument("--streamk", action="store_true",
                     help="call fa_fwd_ws with a workspace (stream-K split of full attention)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,

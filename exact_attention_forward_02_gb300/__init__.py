@@ -25,7 +25,7 @@ STATUS = {
     0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_HEAD_DIM", -3: "FA_ERR_SHAPE",
     -4: "FA_ERR_EMPTY_KEYS", -5: "FA_ERR_SCALE", -6: "FA_ERR_ALIGN", -7: "FA_ERR_DTYPE",
     -8: "FA_ERR_CUDA", -9: "FA_ERR_TENSOR_MAP", -10: "FA_ERR_DEVICE", -11: "FA_ERR_TIMEOUT",
-    -12: "FA_ERR_WORKSPACE", -13: "FA_ERR_SCRATCH_LIMIT",
+    -12: "FA_ERR_WORKSPACE", -13: "FA_ERR_SCRATCH_LIMIT", -14: "FA_ERR_DROPOUT",
 }
 FA_NOALLOC_SCRATCH_BYTES = 48 << 20
 globals().update({v: k for k, v in STATUS.items()})
@@ -53,6 +53,13 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_fwd_dropout.restype = ctypes.c_int
+    lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
+        ctypes.c_uint, vp]
+    lib.fa_dropout_mask.restype = ctypes.c_int
+    lib.fa_dropout_mask.argtypes = [vp] + [ctypes.c_int] * 4 + [
+        ctypes.c_float, ctypes.c_ulonglong, ctypes.c_uint, vp]
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd.argtypes = [vp] * 9 + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
@@ -98,6 +105,20 @@ def fa_fwd_noalloc(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream)
     """C-ABI call of the allocation-free variant (fixed device scratch, see fa_fwd.h)."""
     return int(lib.fa_fwd_noalloc(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
                                   float(scale), int(bool(causal)), int(dtype), stream))
+
+
+def fa_fwd_dropout(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset,
+                   stream) -> int:
+    """C-ABI call of the forward pass with dropout (mask of (seed, offset), see fa_fwd.h)."""
+    return int(lib.fa_fwd_dropout(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
+                                  float(scale), int(bool(causal)), int(dtype), float(p_drop),
+                                  int(seed), int(offset), stream))
+
+
+def fa_dropout_mask(keep, B, H, Nq, Nk, p_drop, seed, offset, stream) -> int:
+    """C-ABI call writing the keep mask [B,H,Nq,Nk] (bytes) of fa_fwd_dropout."""
+    return int(lib.fa_dropout_mask(keep, int(B), int(H), int(Nq), int(Nk), float(p_drop),
+                                   int(seed), int(offset), stream))
 
 
 def fa_fwd_workspace_bytes(B, H, Nq, Nk, d, causal) -> int:

@@ -10,13 +10,18 @@
 //     O~   = exp(m - m') O~ + P V_j
 // and finally O = O~ / l, L = m + ln l. The scores never leave the SM.
 //
-// GB300 mapping (one persistent CTA per SM, 11 warps):
+// With dropout ("Flash Attention" page, "Algorithm 2") the P fed to the second product is
+// masked by the Philox mask of philox.cuh, l stays the sum of the undropped P, and the
+// epilogue divides by l (1 - p).
+//
+// GB300 mapping (one persistent CTA per SM, 12 warps):
 //   warp 8      TMA producer: loads the two 128-row Q tiles of a work item once, then
 //               streams K_j, V_j through a ring of shared-memory slots (mbarrier pipeline).
-//   warps 9,10  MMA issuers, one per Q tile: one thread each issues tcgen05.mma for
-//               S = Q K^T (both operands K-major in shared memory, fp32 accumulator in
-//               Tensor Memory) and O~ += P V (P read from Tensor Memory, V MN-major in
-//               shared memory), and signals completion with tcgen05.commit.
+//   warp 9      MMA issuer for both Q tiles (warp-converged, one elected lane): issues
+//               tcgen05.mma for S = Q K^T (both operands K-major in shared memory, fp32
+//               accumulator in Tensor Memory) and O~ += P V (P read from Tensor Memory,
+//               V MN-major in shared memory), and signals completion with tcgen05.commit.
+//   warps 10,11 no role (they keep the register split of whole warpgroups).
 //   warps 0-7   two softmax warpgroups, one per Q tile (ping-pong): thread r owns query
 //               row r of its tile (TMEM lane r), reads its 128 scores with tcgen05.ld,
 //               applies the mask, keeps (m, l) in registers in base-2 units (the scale is
@@ -34,6 +39,7 @@
 
 #include "fa_fwd.h"
 #include "sm103_ptx.cuh"
+#include "philox.cuh"
 
 // Device-side status word (one per device that loads the library).
 __device__ int g_fa_status;
@@ -95,6 +101,10 @@ struct Params {
   int n_kv_all;    // ceil(Nk / 128)
   float c;         // scale * log2(e)
   unsigned long long wait_limit_ns;
+  // dropout (kernels instantiated with DROP only)
+  uint32_t drop_bias;    // (0x8000 - t) * 0x00010001 for the 15-bit threshold t
+  uint32_t drop_k0, drop_k1, drop_offset;  // generator key (seed) and counter word 3
+  float drop_rscale;     // 32768 / (32768 - t)
   // stream-K split of the key range (full attention with a workspace): the flattened
   // (item, K/V tile) sequence is cut into gridDim.x equal contiguous ranges
   int streamk;
@@ -237,7 +247,7 @@ __device__ __forceinline__ bool sched_next(Sched& s, Item& it, const Params& p) 
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -535,6 +545,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t c2 = f2(c, c), nb2 = f2(nb, nb);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[2][32];
+        // dropout: the generator words of keys [8g, 8g + 8) of this tile; l keeps the
+        // undropped sum, only the 16-bit P of the second product is masked
+        const uint32_t g_base = (uint32_t)(it.j0 + j) * (BN / 8);
+        uint4 rnd = make_uint4(0, 0, 0, 0);
+        auto drop_pair = [&](int k, uint32_t w) -> uint32_t {
+          if constexpr (DROP) {
+            if ((k & 3) == 0)
+              rnd = dropout_words(g_base + (uint32_t)(k >> 2), (uint32_t)row, (uint32_t)it.bh,
+                                  p.drop_offset, p.drop_k0, p.drop_k1);
+            return w & keep_mask2(uint4_word(rnd, k & 3), p.drop_bias);
+          } else {
+            return w;
+          }
+        };
         // two branch-free copies of the loop (full tile / masked tile) so that the
         // scheduler can overlap the exponentials of many iterations
         if (full) {
@@ -544,7 +568,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
             const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
             acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
-            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+            pk[k >> 5][k & 31] = drop_pair(k, pack2<BF16>(p0, p1));
           }
         } else {
 #pragma unroll
@@ -554,7 +578,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float p0 = 2 * k < vis ? ex2_approx(t0) : 0.f;
             const float p1 = 2 * k + 1 < vis ? ex2_approx(t1) : 0.f;
             acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
-            pk[k >> 5][k & 31] = pack2<BF16>(p0, p1);
+            pk[k >> 5][k & 31] = drop_pair(k, pack2<BF16>(p0, p1));
           }
         }
         float ls;
@@ -605,8 +629,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const bool valid = row < p.Nq;
         if (!it.partial) {
-          // O = O~ / l, L = (m + log2 l) ln 2
-          const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          // O = O~ / l (with dropout O~ / (l (1 - p))), L = (m + log2 l) ln 2
+          float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          if constexpr (DROP) inv_l *= p.drop_rscale;
           uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
                           ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
 #pragma unroll
@@ -675,7 +700,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float2 ml = __ldcg(reinterpret_cast<const float2*>(piece_row(cc) + D));
               l += ml.y * ex2_approx(ml.x - m);
             }
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            float inv_l = l > 0.f ? 1.f / l : 0.f;
+            if constexpr (DROP) inv_l *= p.drop_rscale;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
                             ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
 #pragma unroll 1
@@ -779,7 +805,7 @@ int make_map(CUtensorMap* m, const void* base, int d, int N, int BH, bool bf16) 
 struct DeviceInfo {
   int sms = 0;
   bool ok = false;
-  bool attr_set[2][2][2] = {};
+  bool attr_set[2][2][2][2] = {};
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -804,14 +830,14 @@ int device_info(DeviceInfo** out) {
   return FA_OK;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
            DeviceInfo* di, int grid, cudaStream_t st) {
   using LY = Layout<D>;
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, DROP>;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    bool& set = di->attr_set[D == 128][BF16][CAUSAL];
+    bool& set = di->attr_set[D == 128][BF16][CAUSAL][DROP];
     if (!set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) !=
           cudaSuccess)
@@ -863,9 +889,42 @@ int check_args(const void* Q, const void* K, const void* V, void* O, float* L, i
   return FA_OK;
 }
 
+// Dropout arguments after the host checks: the 15-bit threshold t (> 0), seed and offset.
+struct DropArgs {
+  uint32_t t;
+  unsigned long long seed;
+  unsigned int offset;
+};
+
+// The 15-bit threshold of the dropout probability: t = round(p * 32768); false when p is
+// negative, not finite, or so close to 1 that t would be 32768 (every entry dropped).
+bool dropout_threshold(float p_drop, uint32_t* t) {
+  if (!(p_drop >= 0.f) || !isfinite(p_drop)) return false;
+  const double tt = floor((double)p_drop * 32768.0 + 0.5);
+  if (tt >= 32768.0) return false;
+  *t = (uint32_t)tt;
+  return true;
+}
+
+template <bool DROP>
+int dispatch(int d, bool bf16, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+             const CUtensorMap& mv, const Params& p, DeviceInfo* di, int grid, cudaStream_t st) {
+  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch<64, false, false, DROP>(mq, mk, mv, p, di, grid, st);
+    case 1: return launch<64, false, true, DROP>(mq, mk, mv, p, di, grid, st);
+    case 2: return launch<64, true, false, DROP>(mq, mk, mv, p, di, grid, st);
+    case 3: return launch<64, true, true, DROP>(mq, mk, mv, p, di, grid, st);
+    case 4: return launch<128, false, false, DROP>(mq, mk, mv, p, di, grid, st);
+    case 5: return launch<128, false, true, DROP>(mq, mk, mv, p, di, grid, st);
+    case 6: return launch<128, true, false, DROP>(mq, mk, mv, p, di, grid, st);
+    default: return launch<128, true, true, DROP>(mq, mk, mv, p, di, grid, st);
+  }
+}
+
 int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq,
         int Nk, int d, float scale, int causal, fa_dtype dtype, void* workspace,
-        size_t workspace_bytes, bool use_ws, void* stream) {
+        size_t workspace_bytes, bool use_ws, void* stream, const DropArgs* drop = nullptr) {
   bool noop = false;
   int rc = check_args(Q, K, V, O, L, B, H, Nq, Nk, d, scale, dtype, &noop);
   if (rc != FA_OK || noop) return rc;
@@ -902,6 +961,17 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
     grid = w.G;
   }
 
+  p.drop_bias = 0;
+  p.drop_k0 = p.drop_k1 = p.drop_offset = 0;
+  p.drop_rscale = 1.f;
+  if (drop) {
+    p.drop_bias = (0x8000u - drop->t) * 0x00010001u;
+    p.drop_k0 = (uint32_t)(drop->seed & 0xFFFFFFFFull);
+    p.drop_k1 = (uint32_t)(drop->seed >> 32);
+    p.drop_offset = drop->offset;
+    p.drop_rscale = (float)(32768.0 / (32768.0 - (double)drop->t));
+  }
+
   const bool bf16 = dtype == FA_BF16;
   CUtensorMap mq, mk, mv;
   if ((rc = make_map(&mq, Q, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
@@ -909,16 +979,27 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   if ((rc = make_map(&mv, V, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
-  switch (key) {
-    case 0: return launch<64, false, false>(mq, mk, mv, p, di, grid, st);
-    case 1: return launch<64, false, true>(mq, mk, mv, p, di, grid, st);
-    case 2: return launch<64, true, false>(mq, mk, mv, p, di, grid, st);
-    case 3: return launch<64, true, true>(mq, mk, mv, p, di, grid, st);
-    case 4: return launch<128, false, false>(mq, mk, mv, p, di, grid, st);
-    case 5: return launch<128, false, true>(mq, mk, mv, p, di, grid, st);
-    case 6: return launch<128, true, false>(mq, mk, mv, p, di, grid, st);
-    default: return launch<128, true, true>(mq, mk, mv, p, di, grid, st);
+  return drop ? dispatch<true>(d, bf16, causal, mq, mk, mv, p, di, grid, st)
+              : dispatch<false>(d, bf16, causal, mq, mk, mv, p, di, grid, st);
+}
+
+// One thread per (row, group of 8 keys): the keep bytes of the dropout mask, computed by
+// the same device functions the attention kernel uses.
+__global__ void fa_dropout_mask_kernel(uint8_t* keep, long long rows, int Nq, int Nk, int groups,
+                                       uint32_t bias, uint32_t k0, uint32_t k1, uint32_t offset) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= rows * groups) return;
+  const long long r = t / groups;
+  const int g = (int)(t % groups);
+  const uint32_t bh = (uint32_t)(r / Nq), i = (uint32_t)(r % Nq);
+  const uint4 w = fa::dropout_words((uint32_t)g, i, bh, offset, k0, k1);
+  uint8_t* dst = keep + r * Nk;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t m = fa::keep_mask2(fa::uint4_word(w, q), bias);
+    const int j = 8 * g + 2 * q;
+    if (j < Nk) dst[j] = (uint8_t)(m & 1u);
+    if (j + 1 < Nk) dst[j + 1] = (uint8_t)(m >> 31);
   }
 }
 
@@ -1026,6 +1107,41 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
              (size_t)FA_NOALLOC_SCRATCH_BYTES, true, stream);
 }
 
+int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                   int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype, float p_drop,
+                   unsigned long long seed, unsigned int offset, void* stream) {
+  uint32_t t = 0;
+  if (!dropout_threshold(p_drop, &t)) return FA_ERR_DROPOUT;
+  if (t == 0)  // nothing is dropped: the plain forward pass
+    return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, nullptr, 0, false, stream);
+  const DropArgs da{t, seed, offset};
+  return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, nullptr, 0, false, stream, &da);
+}
+
+int fa_dropout_mask(unsigned char* keep, int B, int H, int Nq, int Nk, float p_drop,
+                    unsigned long long seed, unsigned int offset, void* stream) {
+  uint32_t t = 0;
+  if (!dropout_threshold(p_drop, &t)) return FA_ERR_DROPOUT;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  const long long rows = (long long)B * H * Nq;
+  if (rows == 0 || Nk == 0) return FA_OK;
+  if ((long long)B * H > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (!keep) return FA_ERR_NULL;
+  const int groups = (Nk + 7) / 8;
+  const long long threads = rows * groups;
+  const int block = 256;
+  const long long grid = (threads + block - 1) / block;
+  if (grid > 0x7fffffffLL) return FA_ERR_SHAPE;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc != FA_OK) return rc;
+  fa_dropout_mask_kernel<<<(unsigned)grid, block, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      keep, rows, Nq, Nk, groups, (0x8000u - t) * 0x00010001u, (uint32_t)(seed & 0xFFFFFFFFull),
+      (uint32_t)(seed >> 32), offset);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
   return bwd_ws_bytes((long long)B * H, Nq);
@@ -1116,6 +1232,8 @@ const char* fa_strerror(int code) {
     case FA_ERR_WORKSPACE: return "workspace missing or smaller than fa_fwd_workspace_bytes()";
     case FA_ERR_SCRATCH_LIMIT:
       return "the problem needs more scratch than fa_fwd_noalloc's fixed array (FA_NOALLOC_SCRATCH_BYTES)";
+    case FA_ERR_DROPOUT:
+      return "dropout probability must be finite, >= 0 and below 1 - 2^-16";
     default: return "unknown status code";
   }
 }

@@ -42,7 +42,8 @@ enum {
   FA_ERR_DEVICE = -10,     /* the current device is not an sm_103 GPU                     */
   FA_ERR_TIMEOUT = -11,    /* device-side: a pipeline wait exceeded its time limit        */
   FA_ERR_WORKSPACE = -12,  /* fa_fwd_ws: workspace missing or too small                   */
-  FA_ERR_SCRATCH_LIMIT = -13 /* fa_fwd_noalloc: needs more than FA_NOALLOC_SCRATCH_BYTES   */
+  FA_ERR_SCRATCH_LIMIT = -13, /* fa_fwd_noalloc: needs more than FA_NOALLOC_SCRATCH_BYTES  */
+  FA_ERR_DROPOUT = -14     /* dropout probability negative, not finite or too close to 1  */
 };
 
 /* Size of the fixed device scratch array behind fa_fwd_noalloc (48 MiB). */
@@ -125,6 +126,36 @@ int fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* L,
 int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* L,
                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    fa_dtype dtype, void* stream);
+
+/* fa_fwd_dropout -- the forward pass with dropout on the attention probabilities
+ * ("Flash Attention" page, "Algorithm 2": P_dropped = dropout(P, p_drop), O = P_dropped V;
+ * the forward returns the generator state, here the pair (seed, offset)):
+ *     O[b,h,i,:] = sum_j P_ij Z_ij V[b,h,j,:],   L as in fa_fwd (undropped logsumexp)
+ * with Z_ij = 32768 / (32768 - t) when element (i, j) is kept and 0 when it is dropped.
+ * The mask (the pages name no generator; this is the library's definition):
+ *   t = floor(p_drop * 32768 + 0.5), a 15-bit threshold (p_drop is used to 2^-15);
+ *   with bh = b*H + h, the counter-based generator Philox-4x32-10 (Salmon, Moraes, Dror,
+ *   Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) is evaluated at
+ *     counter (j >> 3, i, bh, offset), key (seed & 0xFFFFFFFF, seed >> 32)
+ *   giving four 32-bit words w[0..3]; x = w[(j >> 1) & 3] for even j, w[(j >> 1) & 3] >> 16
+ *   for odd j, keeping only the low 15 bits; element (i, j) is kept iff x >= t.
+ * Calls with the same (seed, offset) and sizes draw the same mask; use a new offset (or
+ * seed) for every call that needs an independent mask.
+ * Arguments, layout, ownership and errors as fa_fwd, plus FA_ERR_DROPOUT when p_drop is
+ * negative, NaN, infinite, or at least 1 - 2^-16 (t would be 32768: nothing kept).
+ * p_drop small enough that t = 0 runs fa_fwd (nothing dropped, identical results). */
+int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* L,
+                   int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   fa_dtype dtype, float p_drop, unsigned long long seed, unsigned int offset,
+                   void* stream);
+
+/* fa_dropout_mask -- write the keep mask that fa_fwd_dropout uses for these arguments:
+ * keep [B, H, Nq, Nk] bytes (DEVICE pointer, caller-owned), 1 = kept, 0 = dropped.
+ * Causality does not enter the mask (masked-out keys have P = 0 either way). One kernel
+ * on `stream`; same mask definition and errors as fa_fwd_dropout (FA_ERR_NULL for a NULL
+ * `keep` when there is something to write; sizes of 0 are a no-op). */
+int fa_dropout_mask(unsigned char* keep, int B, int H, int Nq, int Nk, float p_drop,
+                    unsigned long long seed, unsigned int offset, void* stream);
 
 /* fa_bwd -- gradients of the forward pass: dQ, dK, dV for the upstream gradient dO
  * (CS336 lecture 5 "05_flash_attention.py", part 3, flash_attention_backward; "Flash

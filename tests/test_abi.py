@@ -105,3 +105,20 @@ def test_backward_host_checks():
     assert fa.fa_bwd(*base, P + 4, 1 << 20, None) == fa.FA_ERR_ALIGN
     assert fa.fa_bwd_workspace_bytes(2, 3, 100, 50, 64) == 2 * 3 * 100 * 4 + (256 - (2 * 3 * 100 * 4) % 256) % 256
     assert fa.fa_bwd_workspace_bytes(2, 3, 100, 50, 96) == 0
+
+
+def test_dropout_host_checks():
+    import exact_attention_forward_02_gb300 as fa
+    base = (P, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1)
+    for bad in (1.0, 1 - 2.0 ** -17, 2.0, -1e-3, float("nan"), float("inf"), -float("inf")):
+        assert fa.fa_fwd_dropout(*base, bad, 1, 2, None) == fa.FA_ERR_DROPOUT, bad
+        assert fa.fa_dropout_mask(P, 1, 1, 8, 8, bad, 1, 2, None) == fa.FA_ERR_DROPOUT, bad
+    # the forward's own checks still apply with a valid probability
+    assert fa.fa_fwd_dropout(0, *base[1:], 0.1, 1, 2, None) == fa.FA_ERR_NULL
+    assert fa.fa_fwd_dropout(*base[:9], 96, *base[10:], 0.1, 1, 2, None) == fa.FA_ERR_HEAD_DIM
+    assert fa.fa_fwd_dropout(*base[:10], float("nan"), *base[11:], 0.1, 1, 2, None) == fa.FA_ERR_SCALE
+    # nothing to do: no-ops that touch no pointer
+    assert fa.fa_fwd_dropout(0, 0, 0, 0, 0, 0, 1, 128, 128, 64, 0.125, 0, 1, 0.1, 1, 2, None) == fa.FA_OK
+    assert fa.fa_dropout_mask(0, 1, 1, 0, 8, 0.1, 1, 2, None) == fa.FA_OK
+    assert fa.fa_dropout_mask(0, 1, 1, 8, 8, 0.1, 1, 2, None) == fa.FA_ERR_NULL
+    assert fa.fa_dropout_mask(P, -1, 1, 8, 8, 0.1, 1, 2, None) == fa.FA_ERR_SHAPE
