@@ -102,9 +102,10 @@ struct Params {
   float c;         // scale * log2(e)
   unsigned long long wait_limit_ns;
   // dropout (kernels instantiated with DROP only)
-  uint32_t drop_bias;    // (0x8000 - t) * 0x00010001 for the 15-bit threshold t
-  uint32_t drop_k0, drop_k1, drop_offset;  // generator key (seed) and counter word 3
-  float drop_rscale;     // 32768 / (32768 - t)
+  uint32_t drop_bias;    // (0x100 - t) * 0x00010001 for the 8-bit threshold t
+  uint32_t drop_offset;  // counter word 3
+  float drop_rscale;     // 256 / (256 - t)
+  PhiloxKeys drop_keys;  // round keys of the seed
   // stream-K split of the key range (full attention with a workspace): the flattened
   // (item, K/V tile) sequence is cut into gridDim.x equal contiguous ranges
   int streamk;
@@ -501,6 +502,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, kv_lim) visible
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < it.n_kv; ++j) {
+        // dropout: the keep bits of this row for K/V tile j, drawn before S_g(j) is ready
+        // (they do not depend on it), so the generator runs while this warpgroup would
+        // otherwise wait for the tensor core
+        uint32_t kbits[4] = {0, 0, 0, 0};
+        if constexpr (DROP)
+          dropout_row_bits((uint32_t)(it.j0 + j) * (BN / 16), (uint32_t)row, (uint32_t)it.bh,
+                           p.drop_offset, p.drop_keys, p.drop_bias, kbits);
         // S_g(j) ready; for j > 0 this also means PV_g(j-1) has completed
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full[g]), s_ph, abort_flag, lim));
         if (!ok) break;
@@ -545,16 +553,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t c2 = f2(c, c), nb2 = f2(nb, nb);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[2][32];
-        // dropout: the generator words of keys [8g, 8g + 8) of this tile; l keeps the
-        // undropped sum, only the 16-bit P of the second product is masked
-        const uint32_t g_base = (uint32_t)(it.j0 + j) * (BN / 8);
-        uint4 rnd = make_uint4(0, 0, 0, 0);
+        // dropout: l keeps the undropped sum; only the 16-bit P of the second product is
+        // masked, pair k by the bits (k & 15, 16 + (k & 15)) of kbits[k >> 4]
         auto drop_pair = [&](int k, uint32_t w) -> uint32_t {
           if constexpr (DROP) {
-            if ((k & 3) == 0)
-              rnd = dropout_words(g_base + (uint32_t)(k >> 2), (uint32_t)row, (uint32_t)it.bh,
-                                  p.drop_offset, p.drop_k0, p.drop_k1);
-            return w & keep_mask2(uint4_word(rnd, k & 3), p.drop_bias);
+            return w & pair_mask(kbits[k >> 4], k & 15);
           } else {
             return w;
           }
@@ -889,22 +892,24 @@ int check_args(const void* Q, const void* K, const void* V, void* O, float* L, i
   return FA_OK;
 }
 
-// Dropout arguments after the host checks: the 15-bit threshold t (> 0), seed and offset.
+// Dropout arguments after the host checks: the 8-bit threshold t (> 0), seed and offset.
 struct DropArgs {
   uint32_t t;
   unsigned long long seed;
   unsigned int offset;
 };
 
-// The 15-bit threshold of the dropout probability: t = round(p * 32768); false when p is
-// negative, not finite, or so close to 1 that t would be 32768 (every entry dropped).
+// The 8-bit threshold of the dropout probability: t = round(p * 256); false when p is
+// negative, not finite, or so close to 1 that t would be 256 (every entry dropped).
 bool dropout_threshold(float p_drop, uint32_t* t) {
   if (!(p_drop >= 0.f) || !isfinite(p_drop)) return false;
-  const double tt = floor((double)p_drop * 32768.0 + 0.5);
-  if (tt >= 32768.0) return false;
+  const double tt = floor((double)p_drop * 256.0 + 0.5);
+  if (tt >= 256.0) return false;
   *t = (uint32_t)tt;
   return true;
 }
+
+uint32_t dropout_bias(uint32_t t) { return (0x100u - t) * 0x00010001u; }
 
 template <bool DROP>
 int dispatch(int d, bool bf16, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
@@ -962,14 +967,14 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   }
 
   p.drop_bias = 0;
-  p.drop_k0 = p.drop_k1 = p.drop_offset = 0;
+  p.drop_offset = 0;
   p.drop_rscale = 1.f;
+  p.drop_keys = philox_keys(0);
   if (drop) {
-    p.drop_bias = (0x8000u - drop->t) * 0x00010001u;
-    p.drop_k0 = (uint32_t)(drop->seed & 0xFFFFFFFFull);
-    p.drop_k1 = (uint32_t)(drop->seed >> 32);
+    p.drop_bias = dropout_bias(drop->t);
+    p.drop_keys = philox_keys(drop->seed);
     p.drop_offset = drop->offset;
-    p.drop_rscale = (float)(32768.0 / (32768.0 - (double)drop->t));
+    p.drop_rscale = (float)(256.0 / (256.0 - (double)drop->t));
   }
 
   const bool bf16 = dtype == FA_BF16;
@@ -983,23 +988,28 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
               : dispatch<false>(d, bf16, causal, mq, mk, mv, p, di, grid, st);
 }
 
-// One thread per (row, group of 8 keys): the keep bytes of the dropout mask, computed by
+// One thread per (row, group of 16 keys): the keep bytes of the dropout mask, computed by
 // the same device functions the attention kernel uses.
 __global__ void fa_dropout_mask_kernel(uint8_t* keep, long long rows, int Nq, int Nk, int groups,
-                                       uint32_t bias, uint32_t k0, uint32_t k1, uint32_t offset) {
+                                       uint32_t bias, const __grid_constant__ PhiloxKeys keys,
+                                       uint32_t offset) {
   const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= rows * groups) return;
   const long long r = t / groups;
   const int g = (int)(t % groups);
   const uint32_t bh = (uint32_t)(r / Nq), i = (uint32_t)(r % Nq);
-  const uint4 w = fa::dropout_words((uint32_t)g, i, bh, offset, k0, k1);
+  const uint4 w = fa::dropout_words((uint32_t)g, i, bh, offset, keys);
   uint8_t* dst = keep + r * Nk;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t m = fa::keep_mask2(fa::uint4_word(w, q), bias);
-    const int j = 8 * g + 2 * q;
-    if (j < Nk) dst[j] = (uint8_t)(m & 1u);
-    if (j + 1 < Nk) dst[j + 1] = (uint8_t)(m >> 31);
+  for (int m = 0; m < 4; ++m) {
+    uint32_t f0, f1;
+    fa::keep_flags4(fa::uint4_word(w, m), bias, f0, f1);
+    const uint32_t flag[4] = {(f0 >> 8) & 1u, (f0 >> 24) & 1u, (f1 >> 8) & 1u, (f1 >> 24) & 1u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = 16 * g + 4 * m + e;
+      if (j < Nk) dst[j] = (uint8_t)flag[e];
+    }
   }
 }
 
@@ -1127,7 +1137,7 @@ int fa_dropout_mask(unsigned char* keep, int B, int H, int Nq, int Nk, float p_d
   if (rows == 0 || Nk == 0) return FA_OK;
   if ((long long)B * H > 0x7fffffffLL) return FA_ERR_SHAPE;
   if (!keep) return FA_ERR_NULL;
-  const int groups = (Nk + 7) / 8;
+  const int groups = (Nk + 15) / 16;
   const long long threads = rows * groups;
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
@@ -1136,8 +1146,7 @@ int fa_dropout_mask(unsigned char* keep, int B, int H, int Nq, int Nk, float p_d
   int rc = device_info(&di);
   if (rc != FA_OK) return rc;
   fa_dropout_mask_kernel<<<(unsigned)grid, block, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      keep, rows, Nq, Nk, groups, (0x8000u - t) * 0x00010001u, (uint32_t)(seed & 0xFFFFFFFFull),
-      (uint32_t)(seed >> 32), offset);
+      keep, rows, Nq, Nk, groups, dropout_bias(t), philox_keys(seed), offset);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -1233,7 +1242,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_SCRATCH_LIMIT:
       return "the problem needs more scratch than fa_fwd_noalloc's fixed array (FA_NOALLOC_SCRATCH_BYTES)";
     case FA_ERR_DROPOUT:
-      return "dropout probability must be finite, >= 0 and below 1 - 2^-16";
+      return "dropout probability must be finite, >= 0 and below 1 - 2^-9";
     default: return "unknown status code";
   }
 }

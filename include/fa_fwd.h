@@ -131,18 +131,19 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
  * ("Flash Attention" page, "Algorithm 2": P_dropped = dropout(P, p_drop), O = P_dropped V;
  * the forward returns the generator state, here the pair (seed, offset)):
  *     O[b,h,i,:] = sum_j P_ij Z_ij V[b,h,j,:],   L as in fa_fwd (undropped logsumexp)
- * with Z_ij = 32768 / (32768 - t) when element (i, j) is kept and 0 when it is dropped.
+ * with Z_ij = 256 / (256 - t) when element (i, j) is kept and 0 when it is dropped.
  * The mask (the pages name no generator; this is the library's definition):
- *   t = floor(p_drop * 32768 + 0.5), a 15-bit threshold (p_drop is used to 2^-15);
+ *   t = floor(p_drop * 256 + 0.5), an 8-bit threshold (p_drop is used to 1/256);
  *   with bh = b*H + h, the counter-based generator Philox-4x32-10 (Salmon, Moraes, Dror,
  *   Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) is evaluated at
- *     counter (j >> 3, i, bh, offset), key (seed & 0xFFFFFFFF, seed >> 32)
- *   giving four 32-bit words w[0..3]; x = w[(j >> 1) & 3] for even j, w[(j >> 1) & 3] >> 16
- *   for odd j, keeping only the low 15 bits; element (i, j) is kept iff x >= t.
+ *     counter (j >> 4, i, bh, offset), key (seed & 0xFFFFFFFF, seed >> 32)
+ *   giving four 32-bit words w[0..3]; key j draws the byte x = byte number
+ *   2 (j & 1) + ((j >> 1) & 1) of w[(j >> 2) & 3] (bytes counted from the least
+ *   significant), and element (i, j) is kept iff x >= t.
  * Calls with the same (seed, offset) and sizes draw the same mask; use a new offset (or
  * seed) for every call that needs an independent mask.
  * Arguments, layout, ownership and errors as fa_fwd, plus FA_ERR_DROPOUT when p_drop is
- * negative, NaN, infinite, or at least 1 - 2^-16 (t would be 32768: nothing kept).
+ * negative, NaN, infinite, or at least 1 - 2^-9 (t would be 256: nothing kept).
  * p_drop small enough that t = 0 runs fa_fwd (nothing dropped, identical results). */
 int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* L,
                    int B, int H, int Nq, int Nk, int d, float scale, int causal,

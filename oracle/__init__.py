@@ -248,7 +248,7 @@ def philox4x32_10(ctr, key):
 
 
 def dropout_threshold(p_drop: float) -> int:
-    """The 15-bit threshold t of p_drop, or -1 when p_drop is out of range."""
+    """The 8-bit threshold t of p_drop, or -1 when p_drop is out of range."""
     return int(_load().fa_oracle_dropout_threshold(float(p_drop)))
 
 

@@ -109,25 +109,27 @@ void philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]
 // The dropout mask Z of [CA-2]. The pages fix dropout(P, p) (each probability kept with
 // probability 1 - p and then divided by 1 - p, so that E[P_dropped] = P) but name no
 // generator or counter layout; this is the library's definition of both:
-//   threshold t = floor(p * 32768 + 0.5), a 15-bit integer (p is used to 2^-15);
+//   threshold t = floor(p * 256 + 0.5), an 8-bit integer (p is used to 1/256);
 //   for element (bh, i, j) = (b*H + h, query row, key):
-//     words = Philox-4x32-10(counter = (j >> 3, i, bh, offset),
+//     words = Philox-4x32-10(counter = (j >> 4, i, bh, offset),
 //                            key = (seed mod 2^32, seed div 2^32))
-//     w = words[(j >> 1) & 3];  x = the low 15 bits of w (j even) or of w >> 16 (j odd)
-//     keep = (x >= t);  Z_ij = keep ? 32768 / (32768 - t) : 0
-// so one call of the generator serves eight consecutive keys of one query row, and the
-// kept fraction is exactly (32768 - t) / 32768 in expectation.
+//     w = words[(j >> 2) & 3]; the four keys 4m .. 4m+3 of w take, in order, byte 0,
+//     byte 2, byte 1 and byte 3 of w (the low bytes of its two 16-bit halves serve the
+//     first key pair, the high bytes the second): x = byte ((j & 1) * 2 + ((j >> 1) & 1))
+//     keep = (x >= t);  Z_ij = keep ? 256 / (256 - t) : 0
+// so one call of the generator serves sixteen consecutive keys of one query row, and the
+// kept fraction is exactly (256 - t) / 256 in expectation.
 struct Dropout {
     uint32_t t;
     uint32_t key[2];
     uint32_t offset;
-    double z_keep;  // 32768 / (32768 - t)
+    double z_keep;  // 256 / (256 - t)
 };
 
 bool dropout_threshold(double p, uint32_t* t) {
     if (!(p >= 0.0) || !std::isfinite(p)) return false;
-    const double tt = std::floor(p * 32768.0 + 0.5);
-    if (tt >= 32768.0) return false;
+    const double tt = std::floor(p * 256.0 + 0.5);
+    if (tt >= 256.0) return false;
     *t = (uint32_t)tt;
     return true;
 }
@@ -138,16 +140,17 @@ Dropout make_dropout(uint32_t t, uint64_t seed, uint32_t offset) {
     dr.key[0] = (uint32_t)(seed & 0xFFFFFFFFu);
     dr.key[1] = (uint32_t)(seed >> 32);
     dr.offset = offset;
-    dr.z_keep = 32768.0 / (32768.0 - (double)t);
+    dr.z_keep = 256.0 / (256.0 - (double)t);
     return dr;
 }
 
 bool dropout_keep(const Dropout& dr, int64_t bh, int64_t i, int64_t j) {
-    const uint32_t ctr[4] = {(uint32_t)(j >> 3), (uint32_t)i, (uint32_t)bh, dr.offset};
+    const uint32_t ctr[4] = {(uint32_t)(j >> 4), (uint32_t)i, (uint32_t)bh, dr.offset};
     uint32_t w[4];
     philox4x32_10(ctr, dr.key, w);
-    const uint32_t word = w[(j >> 1) & 3];
-    const uint32_t x = ((j & 1) ? (word >> 16) : word) & 0x7FFFu;
+    const uint32_t word = w[(j >> 2) & 3];
+    const int byte = (int)((j & 1) * 2 + ((j >> 1) & 1));
+    const uint32_t x = (word >> (8 * byte)) & 0xFFu;
     return x >= dr.t;
 }
 
@@ -402,7 +405,7 @@ int fa_oracle_attention_bwd(const double* Q, const double* K, const double* V, c
 }
 
 // The backward pass with the dropout mask of seed/offset and probability p_drop
-// ([CA-2]; see attention_bwd). Returns -1 for a p_drop outside [0, 1 - 2^-16).
+// ([CA-2]; see attention_bwd). Returns -1 for a p_drop outside [0, 1 - 2^-9).
 int fa_oracle_attention_bwd_dropout(const double* Q, const double* K, const double* V,
                                     const double* dO, int B, int H, int Nq, int Nk, int d,
                                     double scale, int causal, double p_drop, uint64_t seed,
@@ -419,8 +422,8 @@ void fa_oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t*
   philox4x32_10(ctr, key, out);
 }
 
-// The 15-bit dropout threshold t of p_drop (see Dropout), or -1 when p_drop is negative,
-// not finite, or so close to 1 that t would be 32768.
+// The 8-bit dropout threshold t of p_drop (see Dropout), or -1 when p_drop is negative,
+// not finite, or so close to 1 that t would be 256.
 int fa_oracle_dropout_threshold(double p_drop) {
   uint32_t t;
   return dropout_threshold(p_drop, &t) ? (int)t : -1;

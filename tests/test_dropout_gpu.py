@@ -6,7 +6,7 @@ work, so it is compared bit for bit: directly (fa_dropout_mask against the oracl
 mask), and through the attention kernel itself, where Q = 0 makes every probability equal
 and weighted one-hot values make O spell out the kept bits. The outputs on random inputs
 are compared with the oracle's dropout forward under the forward's tolerances scaled by
-the keep factor 32768 / (32768 - t): every term of O is multiplied by it, and so is the
+the keep factor 256 / (256 - t): every term of O is multiplied by it, and so is the
 rounding error of P that the forward's tolerance covers."""
 import ctypes
 
@@ -41,7 +41,7 @@ def _f32(p):
 def keep_factor(p):
     import oracle
     t = oracle.dropout_threshold(_f32(p))
-    return 32768.0 / (32768 - t)
+    return 256.0 / (256 - t)
 
 
 def run_dropout(w, q, k, v, p, seed, offset, nan_fill=True):
@@ -73,11 +73,12 @@ def gpu_mask(B, H, Nq, Nk, p, seed, offset):
 
 
 MASK_CASES = [
-    (1, 1, 1, 8, 0.5, 0, 0),
+    (1, 1, 1, 16, 0.5, 0, 0),
     (2, 3, 37, 45, 0.1, 12345, 7),
     (1, 2, 300, 257, 0.5, (1 << 63) + 99, 0xFFFFFFFF),
     (4, 12, 5, 4097, 0.9, 2**32 + 5, 3),
-    (1, 1, 64, 64, 1 - 2.0 ** -15, 1, 1),
+    (1, 1, 64, 64, 1 - 2.0 ** -8, 1, 1),
+    (2, 2, 129, 33, 0.0, 3, 4),
 ]
 
 

@@ -8,7 +8,7 @@ Philox-4x32-10 (Salmon et al., SC'11) with the counter layout stated in the orac
 include/fa_fwd.h. What fixes each piece here, other than the oracle itself:
   * the generator: the published known-answer vectors (tests/golden/philox4x32_10_kat.json)
     and Triton's independent tl.philox run by its CPU interpreter;
-  * the counter layout and the 15-bit threshold: mask bits worked out by hand from the
+  * the counter layout and the 8-bit threshold: mask bits worked out by hand from the
     first known-answer vector, and the layout checked against Triton's words;
   * the dropout arithmetic: p = 0 gives the plain forward exactly, L does not depend on
     the mask, the mean over seeds converges to the undropped output (unbiased, within a
@@ -55,8 +55,8 @@ def _triton_words(items):
 def test_philox_matches_triton_and_mask_layout(oracle_mod):
     """Triton's tl.philox (an independent implementation) gives the same words as the
     oracle for arbitrary counters and 64-bit seeds, and the oracle's mask follows the
-    stated layout: counter (j >> 3, i, bh, offset), word (j >> 1) & 3, half j & 1,
-    low 15 bits, keep iff x >= t."""
+    stated layout: counter (j >> 4, i, bh, offset), word (j >> 2) & 3, byte
+    2 (j & 1) + ((j >> 1) & 1), keep iff x >= t."""
     rng = np.random.default_rng(11)
     B, H, Nq, Nk = 2, 3, 5, 37
     seed, offset = (1 << 63) + 987654321, 77
@@ -65,7 +65,7 @@ def test_philox_matches_triton_and_mask_layout(oracle_mod):
     items = []
     for bh in range(B * H):
         for i in range(Nq):
-            for g in range((Nk + 7) // 8):
+            for g in range((Nk + 15) // 16):
                 items.append([g, i, bh, offset, seed])
     extra = [[int(x) for x in rng.integers(0, 2**32, 4)] + [int(rng.integers(0, 2**63))]
              for _ in range(8)]
@@ -76,39 +76,42 @@ def test_philox_matches_triton_and_mask_layout(oracle_mod):
     k = 0
     for bh in range(B * H):
         for i in range(Nq):
-            for g in range((Nk + 7) // 8):
+            for g in range((Nk + 15) // 16):
                 w = words[k]
                 k += 1
-                for j in range(8 * g, min(Nk, 8 * g + 8)):
-                    word = w[(j >> 1) & 3]
-                    x = ((word >> 16) if (j & 1) else word) & 0x7FFF
+                for j in range(16 * g, min(Nk, 16 * g + 16)):
+                    word = w[(j >> 2) & 3]
+                    x = (word >> (8 * (2 * (j & 1) + ((j >> 1) & 1)))) & 0xFF
                     expect[bh // H, bh % H, i, j] = 1 if x >= t else 0
     got = oracle_mod.dropout_keep(B, H, Nq, Nk, p, seed, offset)
     assert np.array_equal(got, expect)
 
 
 def test_mask_bits_from_the_first_known_answer_vector(oracle_mod):
-    """seed 0, offset 0, head 0, row 0, keys 0..7 use counter (0, 0, 0, 0) under key
-    (0, 0), whose words are 6627e8d5 e169c58d bc57ac4c 9b00dbd8. Their 15-bit halves in
-    key order (low half first) are 26837 26151 17805 24937 11340 15447 23512 6912."""
-    halves = [26837, 26151, 17805, 24937, 11340, 15447, 23512, 6912]
-    assert oracle_mod.dropout_threshold(0.5) == 16384
-    got = oracle_mod.dropout_keep(1, 1, 1, 8, 0.5, 0, 0)[0, 0, 0]
-    assert got.tolist() == [1, 1, 1, 1, 0, 0, 1, 0]
-    # a threshold equal to a half keeps that key (x >= t), one above drops it
-    for t in (26151, 26152, 6912, 6913, 1, 0):
-        p = t / 32768.0
+    """seed 0, offset 0, head 0, row 0, keys 0..15 use counter (0, 0, 0, 0) under key
+    (0, 0), whose words are 6627e8d5 e169c58d bc57ac4c 9b00dbd8. Taking bytes 0, 2, 1, 3 of
+    each word in turn, the keys draw
+    d5 27 e8 66 | 8d 69 c5 e1 | 4c 57 ac bc | d8 00 db 9b."""
+    x = [0xd5, 0x27, 0xe8, 0x66, 0x8d, 0x69, 0xc5, 0xe1,
+         0x4c, 0x57, 0xac, 0xbc, 0xd8, 0x00, 0xdb, 0x9b]
+    assert oracle_mod.dropout_threshold(0.5) == 128
+    got = oracle_mod.dropout_keep(1, 1, 1, 16, 0.5, 0, 0)[0, 0, 0]
+    assert got.tolist() == [1, 0, 1, 0, 1, 0, 1, 1, 0, 0, 1, 1, 1, 0, 1, 1]
+    # a threshold equal to a draw keeps that key (x >= t), one above drops it
+    for t in (0x66, 0x67, 0x27, 0x28, 1, 0, 255):
+        p = t / 256.0
         assert oracle_mod.dropout_threshold(p) == t
-        got = oracle_mod.dropout_keep(1, 1, 1, 8, p, 0, 0)[0, 0, 0]
-        assert got.tolist() == [1 if x >= t else 0 for x in halves], t
+        got = oracle_mod.dropout_keep(1, 1, 1, 16, p, 0, 0)[0, 0, 0]
+        assert got.tolist() == [1 if v >= t else 0 for v in x], t
 
 
 def test_threshold_rounding_and_range(oracle_mod):
     assert oracle_mod.dropout_threshold(0.0) == 0
-    assert oracle_mod.dropout_threshold(0.1) == 3277           # 3276.8 rounds up
-    assert oracle_mod.dropout_threshold(0.5) == 16384
-    assert oracle_mod.dropout_threshold(1 - 2.0 ** -15) == 32767
-    for bad in (1.0, 1 - 2.0 ** -16, 1.5, -1e-9, float("nan"), float("inf")):
+    assert oracle_mod.dropout_threshold(0.1) == 26            # 25.6 rounds up
+    assert oracle_mod.dropout_threshold(0.5) == 128
+    assert oracle_mod.dropout_threshold(1 - 2.0 ** -8) == 255
+    assert oracle_mod.dropout_threshold(1.5 / 256) == 2        # ties round up
+    for bad in (1.0, 1 - 2.0 ** -9, 1.5, -1e-9, float("nan"), float("inf")):
         assert oracle_mod.dropout_threshold(bad) == -1, bad
     with pytest.raises(ValueError):
         oracle_mod.dropout_keep(1, 1, 1, 1, 1.0, 0, 0)
@@ -139,7 +142,7 @@ def test_logsumexp_does_not_depend_on_the_mask(oracle_mod, causal):
 
 def test_one_hot_values_read_the_mask_out_of_the_output(oracle_mod):
     """Q = 0 makes every probability 1/Nk; with V_j = e_j (Nk = d) the output is
-    O_ij = keep_ij * 32768 / (32768 - t) / Nk, so O reveals the mask element by element."""
+    O_ij = keep_ij * 256 / (256 - t) / Nk, so O reveals the mask element by element."""
     B, H, Nq, Nk = 2, 2, 9, 16
     Q = np.zeros((B, H, Nq, Nk))
     K = np.random.default_rng(3).standard_normal((B, H, Nk, Nk))
@@ -148,7 +151,7 @@ def test_one_hot_values_read_the_mask_out_of_the_output(oracle_mod):
     t = oracle_mod.dropout_threshold(p)
     O, _ = oracle_mod.attention_dropout(Q, K, V, 1.0, False, p, seed, off)
     keep = oracle_mod.dropout_keep(B, H, Nq, Nk, p, seed, off)
-    assert np.allclose(O, keep * (32768.0 / (32768 - t)) / Nk, rtol=0, atol=1e-15)
+    assert np.allclose(O, keep * (256.0 / (256 - t)) / Nk, rtol=0, atol=1e-15)
 
 
 def test_kept_fraction_is_binomial(oracle_mod):
@@ -156,7 +159,7 @@ def test_kept_fraction_is_binomial(oracle_mod):
     for p, seed, off in ((0.1, 5, 0), (0.5, 6, 1), (0.85, 7, 2)):
         keep = oracle_mod.dropout_keep(B, H, Nq, Nk, p, seed, off)
         n = keep.size
-        q = (32768 - oracle_mod.dropout_threshold(p)) / 32768.0
+        q = (256 - oracle_mod.dropout_threshold(p)) / 256.0
         assert abs(keep.mean() - q) < 6 * math.sqrt(q * (1 - q) / n), (p, keep.mean())
         # different offsets and seeds give different masks
         other = oracle_mod.dropout_keep(B, H, Nq, Nk, p, seed, off + 1)
@@ -176,7 +179,7 @@ def test_dropout_is_unbiased_over_seeds(oracle_mod):
         acc += O1
     mean = acc / n
     P = oracle_mod.probs(Q[0, 0], K[0, 0], scale, False)
-    q = (32768 - oracle_mod.dropout_threshold(p)) / 32768.0
+    q = (256 - oracle_mod.dropout_threshold(p)) / 256.0
     var = (P ** 2) @ (V[0, 0] ** 2) * (1.0 / q - 1.0)
     se = np.sqrt(var / n)
     assert np.all(np.abs(mean[0, 0] - O0[0, 0]) < 6 * se + 1e-12)
@@ -197,7 +200,7 @@ def test_dropout_forward_and_backward_match_torch_autograd(oracle_mod, causal):
     Q, K, V = _qkv(8, B, H, Nq, Nk, d)
     dO = np.random.default_rng(9).standard_normal((B, H, Nq, d))
     scale, p, seed, off = 0.45, 0.3, 4242, 1
-    q = (32768 - oracle_mod.dropout_threshold(p)) / 32768.0
+    q = (256 - oracle_mod.dropout_threshold(p)) / 256.0
     Z = torch.from_numpy(oracle_mod.dropout_keep(B, H, Nq, Nk, p, seed, off).astype(np.float64) / q)
     tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (Q, K, V))
     O_t = _masked_forward_torch(tq, tk, tv, scale, causal, Z)

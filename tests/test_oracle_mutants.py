@@ -44,14 +44,17 @@ MUTANTS = [
     ("philox: second key word not bumped", "k1 += 0xBB67AE85u;", "k1 += 0u;", ["philox_kat"]),
     ("dropout: keep only above the threshold", "return x >= dr.t;", "return x > dr.t;",
      ["dropout_kat_bits"]),
-    ("dropout: halves of a word swapped", "((j & 1) ? (word >> 16) : word)",
-     "((j & 1) ? word : (word >> 16))", ["dropout_kat_bits"]),
+    ("dropout: bytes of a word taken in natural order",
+     "const int byte = (int)((j & 1) * 2 + ((j >> 1) & 1));", "const int byte = (int)(j & 3);",
+     ["dropout_kat_bits"]),
     ("dropout: row and head swapped in the counter",
-     "{(uint32_t)(j >> 3), (uint32_t)i, (uint32_t)bh, dr.offset}",
-     "{(uint32_t)(j >> 3), (uint32_t)bh, (uint32_t)i, dr.offset}", ["dropout_layout"]),
-    ("dropout: threshold truncated", "std::floor(p * 32768.0 + 0.5)", "std::floor(p * 32768.0)",
+     "{(uint32_t)(j >> 4), (uint32_t)i, (uint32_t)bh, dr.offset}",
+     "{(uint32_t)(j >> 4), (uint32_t)bh, (uint32_t)i, dr.offset}", ["dropout_layout"]),
+    ("dropout: eight keys per generator call", "{(uint32_t)(j >> 4), (uint32_t)i,",
+     "{(uint32_t)(j >> 3), (uint32_t)i,", ["dropout_layout"]),
+    ("dropout: threshold truncated", "std::floor(p * 256.0 + 0.5)", "std::floor(p * 256.0)",
      ["dropout_threshold"]),
-    ("dropout: kept entries not rescaled", "dr.z_keep = 32768.0 / (32768.0 - (double)t);",
+    ("dropout: kept entries not rescaled", "dr.z_keep = 256.0 / (256.0 - (double)t);",
      "dr.z_keep = 1.0;", ["dropout_unbiased", "dropout_onehot"]),
     ("dropout backward: dP without the mask", "dprow[(size_t)j] = acc * zrow[(size_t)j];",
      "dprow[(size_t)j] = acc;", ["dropout_torch", "dropout_fd"]),
