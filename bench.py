@@ -35,7 +35,8 @@ DOMINANT = "b2h8_n8192_d128_causal"
 FLUSH_BYTES = 256 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ("exact_attention_forward_02_gb300/csrc/fa_fwd.cu",
-                  "exact_attention_forward_02_gb300/csrc/sm103_ptx.cuh")
+                  "exact_attention_forward_02_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_forward_02_gb300/csrc/philox.cuh")
 
 
 def dist_env():
