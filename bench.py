@@ -32,6 +32,9 @@ METRIC = "attention fwd TFLOPS (bf16, causal & full) and % of GB300 dense tensor
 UNIT = "TFLOPS"
 WORKLOADS = ("b2h8_n4096_d128_full", "b2h8_n8192_d128_causal")
 DOMINANT = "b2h8_n8192_d128_causal"
+FP8_WORKLOADS = ("b2h8_n4096_d128_full_fp8", "b2h8_n8192_d128_causal_fp8")
+FP8_DOMINANT = "b2h8_n8192_d128_causal_fp8"
+FP8_OVER_BF16 = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FLUSH_BYTES = 256 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ("exact_attention_forward_02_gb300/csrc/fa_fwd.cu",
@@ -184,15 +187,21 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
 
-    names = tuple(args.workloads.split(",")) if args.workloads else WORKLOADS
-    wl = [gen.WORKLOADS[n] for n in names]
+    allw = {**gen.WORKLOADS, **gen.FP8_WORKLOADS}
+    names = (tuple(args.workloads.split(",")) if args.workloads else
+             FP8_WORKLOADS if args.fp8 else WORKLOADS)
+    wl = [allw[n] for n in names]
     host = {}
     devbuf = {}
+    fp8ws = {}
     for w in wl:
         q, k, v = gen.make_qkv(w)
         host[w.name] = [t.pin_memory() for t in (q, k, v)]
         qd, kd, vd = (t.to(dev) for t in (q, k, v))
-        O = torch.empty((w.B, w.H, w.Nq, w.d), dtype=q.dtype, device=dev)
+        O = torch.empty((w.B, w.H, w.Nq, w.d), dtype=gen.torch_dtype(w.out_dtype), device=dev)
+        if w.dtype == gen.FP8:
+            fp8ws[w.name] = torch.empty(fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.Nk, w.d),
+                                        dtype=torch.uint8, device=dev)
         L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
         # stream-K workspace for full attention (zero-filled once; calls keep it zeroed),
         # only when --streamk asks for it
@@ -205,8 +214,13 @@ def run_ours(args):
 
     def launch(w):
         qd, kd, vd, O, L, wsp = devbuf[w.name]
-        dt = fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16
-        if args.dropout > 0:
+        dt = fa.FA_BF16 if w.out_dtype == gen.BF16 else fa.FA_F16
+        if w.dtype == gen.FP8:
+            wsf = fp8ws[w.name]
+            rc = fa.fa_fwd_fp8(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(),
+                               L.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal,
+                               1.0, 1.0, 1.0, dt, wsf.data_ptr(), wsf.numel(), sp)
+        elif args.dropout > 0:
             # a fresh mask per call: the offset advances like a training loop's would
             drop_offset[0] += 1
             rc = fa.fa_fwd_dropout(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), O.data_ptr(),
@@ -267,7 +281,7 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, launch, D2H O and L
     ne2e = max(3, min(n, 50))
-    pin_out = {w.name: (torch.empty((w.B, w.H, w.Nq, w.d), dtype=gen.torch_dtype(w.dtype)).pin_memory(),
+    pin_out = {w.name: (torch.empty((w.B, w.H, w.Nq, w.d), dtype=gen.torch_dtype(w.out_dtype)).pin_memory(),
                         torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()) for w in wl}
     h2d = sum(t.numel() * t.element_size() for w in wl for t in host[w.name])
     d2h = sum(t.numel() * t.element_size() for w in wl for t in pin_out[w.name])
@@ -297,8 +311,14 @@ def run_ours(args):
 
     if rank == 0:
         peak, peak_sus, peak_kind = peaks()
-        dominant = DOMINANT if DOMINANT in per else max(per, key=lambda n: statistics.fmean(per[n]))
-        wd = gen.WORKLOADS[dominant]
+        dom_pref = FP8_DOMINANT if args.fp8 else DOMINANT
+        dominant = dom_pref if dom_pref in per else max(per, key=lambda n: statistics.fmean(per[n]))
+        wd = allw[dominant]
+        if wd.dtype == gen.FP8:  # the E4M3 contraction's own peak: measured bf16 x nominal ratio
+            peak = peak * FP8_OVER_BF16
+            peak_kind = f"{peak_kind} bf16 x {FP8_OVER_BF16:g} (nominal E4M3/BF16 ratio), e4m3"
+        else:
+            peak_kind = f"{peak_kind} bf16"
         dom_ms = statistics.fmean(per[dominant])
         achieved = wd.flops / (dom_ms * 1e-3) / 1e12
         clk = clocks.summary() if clocks else None
@@ -319,7 +339,8 @@ def run_ours(args):
                        "shapes": [w.describe() for w in wl],
                        "l2": "flushed before every launch (256 MiB write, outside the events)",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
-                       "entry_point": ("fa_fwd_dropout" if args.dropout > 0 else
+                       "entry_point": ("fa_fwd_fp8 (V^T transpose + attention kernel)" if args.fp8 else
+                                       "fa_fwd_dropout" if args.dropout > 0 else
                                        "fa_fwd_ws (stream-K)" if args.streamk else "fa_fwd"),
                        "dropout": args.dropout,
                        "pct_of_peak": round(100 * value / ws / peak, 1)},
@@ -329,7 +350,7 @@ def run_ours(args):
                                    f"{', dropout' if args.dropout > 0 else ''}> on {dominant}",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
-                         "peak_source": f"{peak_kind} bf16 dense (burst: kernel timed alone)",
+                         "peak_source": f"{peak_kind} dense (burst: kernel timed alone)",
                          "traffic": recorded_traffic(dominant) if args.dropout == 0 else None,
                          "algorithmic_bytes": wd.io_bytes},
             "clocks": clk,
@@ -534,6 +555,8 @@ def main():
                     help="comma-separated workload names (default: the two headline workloads)")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass (fa_bwd) instead of the forward")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time fa_fwd_fp8 on the E4M3 versions of the two d=128 workloads")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="time fa_fwd_dropout with this dropout probability (default: no dropout)")
     ap.add_argument("--streamk", action="store_true",

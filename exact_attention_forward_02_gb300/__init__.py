@@ -57,6 +57,11 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
         ctypes.c_uint, vp]
+    lib.fa_fwd_fp8.restype = ctypes.c_int
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int] + [ctypes.c_float] * 3 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_fwd_fp8_workspace_bytes.argtypes = [ctypes.c_int] * 4
     lib.fa_dropout_mask.restype = ctypes.c_int
     lib.fa_dropout_mask.argtypes = [vp] + [ctypes.c_int] * 4 + [
         ctypes.c_float, ctypes.c_ulonglong, ctypes.c_uint, vp]
@@ -113,6 +118,19 @@ def fa_fwd_dropout(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, p_drop,
     return int(lib.fa_fwd_dropout(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
                                   float(scale), int(bool(causal)), int(dtype), float(p_drop),
                                   int(seed), int(offset), stream))
+
+
+def fa_fwd_fp8(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, q_descale, k_descale, v_descale,
+               out_dtype, workspace, workspace_bytes, stream) -> int:
+    """C-ABI call of the E4M3 forward pass (raw device addresses and sizes)."""
+    return int(lib.fa_fwd_fp8(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
+                              float(scale), int(bool(causal)), float(q_descale), float(k_descale),
+                              float(v_descale), int(out_dtype), workspace, int(workspace_bytes),
+                              stream))
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, Nk, d) -> int:
+    return int(lib.fa_fwd_fp8_workspace_bytes(int(B), int(H), int(Nk), int(d)))
 
 
 def fa_dropout_mask(keep, B, H, Nq, Nk, p_drop, seed, offset, stream) -> int:

@@ -76,11 +76,13 @@ struct Barriers {
   int abort_flag;
 };
 
-template <int D>
+// ESZ: bytes per input element (2 for fp16/bf16, 1 for E4M3)
+template <int D, int ESZ = 2>
 struct Layout {
-  static constexpr int TILE_BYTES = BM * D * 2;       // one Q, K or V tile
+  static constexpr int TILE_BYTES = BM * D * ESZ;     // one Q, K or V tile (V^T for E4M3)
   static constexpr int CHUNK_BYTES = BM * 128;        // 128 rows x one 128-byte swizzle span
-  static constexpr int CHUNKS = D / 64;               // 64 16-bit elements per span
+  static constexpr int CHUNKS = D * ESZ / 128;        // 128-byte spans per row
+  static constexpr int CHUNK_ELEMS = 128 / ESZ;       // elements per span
   static constexpr int FIXED = 2 * TILE_BYTES + 1024 /*align*/ + 512 /*bars*/;
   static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TILE_BYTES;
   static constexpr int KV_SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;
@@ -106,6 +108,7 @@ struct Params {
   uint32_t drop_offset;  // counter word 3
   float drop_rscale;     // 256 / (256 - t)
   PhiloxKeys drop_keys;  // round keys of the seed
+  float o_scale;         // extra factor on O (the V descale of E4M3 inputs; 1 otherwise)
   // stream-K split of the key range (full attention with a workspace): the flattened
   // (item, K/V tile) sequence is cut into gridDim.x equal contiguous ranges
   int streamk;
@@ -248,11 +251,15 @@ __device__ __forceinline__ bool sched_next(Sched& s, Item& it, const Params& p) 
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int D, bool BF16, bool CAUSAL, bool DROP>
+// BF16: type of O (and of Q, K, V unless FP8). FP8: Q, K are E4M3 [BH, N, D] and tmV maps
+// V^T, E4M3 [BH, D, ldvt] (keys contiguous), so that V is a K-major operand of P V.
+template <int D, bool BF16, bool CAUSAL, bool DROP, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using LY = Layout<D>;
+  static_assert(!(FP8 && DROP), "dropout is not combined with E4M3 inputs");
+  static_assert(!FP8 || D == 128, "E4M3 inputs need d = 128 (one 128-byte row per tile row)");
+  using LY = Layout<D, FP8 ? 1 : 2>;
   constexpr int PART_ROW = D + 4;  // O~[D], m, l, 2 pad: rows stay 16-byte aligned
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued_mask = 0, last_par = 0;  // for draining on abort
       bool q_issued = false;
       bool ok = true;
-      auto load_kv = [&](const CUtensorMap* tm, int bh, int row0) -> bool {
+      auto load_kv = [&](const CUtensorMap* tm, int bh, int row0, bool is_v) -> bool {
         const uint32_t slot = ld % LY::KV_SLOTS;
         const uint32_t par = (ld / LY::KV_SLOTS) & 1u;
         if (ld >= (uint32_t)LY::KV_SLOTS) {
@@ -322,9 +329,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t full = smem_u32(&bars->kv_full[slot]);
         mbar_arrive_expect_tx(full, LY::TILE_BYTES);
         const uint32_t dst = sKV + slot * LY::TILE_BYTES;
+        if (FP8 && is_v) {  // V^T tile: D rows (head dims) x 128 keys starting at key row0
+          tma_load_3d_hint(dst, tm, full, row0, 0, bh, pol_kv);
+        } else {
 #pragma unroll
-        for (int c = 0; c < LY::CHUNKS; ++c)
-          tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, tm, full, c * 64, row0, bh, pol_kv);
+          for (int c = 0; c < LY::CHUNKS; ++c)
+            tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, tm, full, c * LY::CHUNK_ELEMS, row0, bh,
+                             pol_kv);
+        }
         issued_mask |= 1u << slot;
         last_par = (last_par & ~(1u << slot)) | (par << slot);
         ++ld;
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Sched sch = sched_begin(p);
       Item it;
       for (int r = 0; ok && sched_next<CAUSAL>(sch, it, p); ++r) {
-        ok = load_kv(&tmK, it.bh, it.j0 * BN);
+        ok = load_kv(&tmK, it.bh, it.j0 * BN, false);
         if (!ok) break;
         ok = wait_bar(smem_u32(&bars->q_empty), q_ph ^ 1, abort_flag, lim);
         if (!ok) break;
@@ -342,18 +354,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(qf, (it.has1 ? 2 : 1) * LY::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < LY::CHUNKS; ++c)
-          tma_load_3d_hint(sQ + c * LY::CHUNK_BYTES, &tmQ, qf, c * 64, it.q0, it.bh, pol_q);
+          tma_load_3d_hint(sQ + c * LY::CHUNK_BYTES, &tmQ, qf, c * LY::CHUNK_ELEMS, it.q0, it.bh,
+                           pol_q);
         if (it.has1) {
 #pragma unroll
           for (int c = 0; c < LY::CHUNKS; ++c)
-            tma_load_3d_hint(sQ + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmQ, qf, c * 64,
-                             it.q0 + BM, it.bh, pol_q);
+            tma_load_3d_hint(sQ + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmQ, qf,
+                             c * LY::CHUNK_ELEMS, it.q0 + BM, it.bh, pol_q);
         }
         q_issued = true;
-        ok = load_kv(&tmV, it.bh, it.j0 * BN);
+        ok = load_kv(&tmV, it.bh, it.j0 * BN, true);
         for (int j = 1; j < it.n_kv && ok; ++j) {
-          ok = load_kv(&tmK, it.bh, (it.j0 + j) * BN);
-          if (ok) ok = load_kv(&tmV, it.bh, (it.j0 + j) * BN);
+          ok = load_kv(&tmK, it.bh, (it.j0 + j) * BN, false);
+          if (ok) ok = load_kv(&tmV, it.bh, (it.j0 + j) * BN, true);
         }
       }
       if (!ok) {
@@ -369,13 +382,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // The whole warp runs this loop converged, so descriptors and counters stay
     // warp-uniform; one elected lane issues each tcgen05.mma / commit.
     {
-      constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BM, BN);
-      constexpr uint32_t ID_O = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BM, D);
+      // E4M3: both operands of both products K-major (V^T tiles), type code 0 = E4M3
+      constexpr uint32_t ID_S = umma_idesc_f16(FP8 ? 0 : (BF16 ? 1 : 0), 0, 0, BM, BN);
+      constexpr uint32_t ID_O = umma_idesc_f16(FP8 ? 0 : (BF16 ? 1 : 0), 0, FP8 ? 0 : 1, BM, D);
       // descriptors are built once; per k-step and per slot only the start-address field
       // (bits 0-13, in 16-byte units) advances, which never carries out of its field
       const uint64_t dQ0 = umma_smem_desc(sQ, 16, 1024);
       const uint64_t dK = umma_smem_desc(sKV, 16, 1024);
-      const uint64_t dV = umma_smem_desc(sKV, LY::CHUNK_BYTES, 1024);
+      const uint64_t dV = FP8 ? umma_smem_desc(sKV, 16, 1024) : umma_smem_desc(sKV, LY::CHUNK_BYTES, 1024);
       uint32_t m = 0;  // global K/V tile counter: K_m is load 2m, V_m is load 2m+1
       uint32_t q_ph = 0;
       uint32_t p_ph[2] = {0, 0};
@@ -391,27 +405,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (elect_one()) umma_commit(smem_u32(bar));
         __syncwarp();
       };
-      // S_g = Q_g K^T : M=128 rows, N=128 keys, K=D (16 per instruction)
+      // S_g = Q_g K^T : M=128 rows, N=128 keys, K=D (32 bytes per instruction: 16
+      // elements of 16 bits, or 32 of E4M3)
       auto issue_s = [&](int g, uint32_t kslot) {
         const uint64_t dq = dQ0 + ((g * LY::TILE_BYTES) >> 4);
         const uint64_t dk = dK + ((kslot * LY::TILE_BYTES) >> 4);
         if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
+          for (int ks = 0; ks < D * (FP8 ? 1 : 2) / 32; ++ks) {
             const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
-            umma_ss(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+            if constexpr (FP8)
+              umma_ss_f8(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+            else
+              umma_ss(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
           }
         }
         __syncwarp();
       };
       // O_g += P_g V : M=128 rows, N=D, K=128 keys; P is read from Tensor Memory
+      // (E4M3: P holds four keys per TMEM column, V^T is K-major: 32 keys per instruction,
+      // 8 TMEM columns and 32 bytes of every V^T row)
       auto issue_pv = [&](int g, uint32_t vslot, bool acc) {
         const uint64_t dv = dV + ((vslot * LY::TILE_BYTES) >> 4);
         if (elect_one()) {
+          if constexpr (FP8) {
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks)
-            umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
-                    dv + ((ks * 16 * 128) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < BN / 32; ++ks)
+              umma_ts_f8(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
+                         dv + ((ks * 32) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+              umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
+                      dv + ((ks * 16 * 128) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+          }
         }
         __syncwarp();
       };
@@ -562,6 +589,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             return w;
           }
         };
+        // P of key pair k (keys 2k, 2k+1) into the packed words of the second product:
+        // two 16-bit values per word, or (E4M3) four 8-bit values per word, lowest key in
+        // the lowest bits; k is a compile-time constant in the unrolled loops below
+        float pe0 = 0.f, pe1 = 0.f;
+        auto emit = [&](int k, float p0, float p1) {
+          if constexpr (FP8) {
+            if ((k & 1) == 0) {
+              pe0 = p0;
+              pe1 = p1;
+            } else {
+              pk[(k >> 1) >> 5][(k >> 1) & 31] = pack4_e4m3(pe0, pe1, p0, p1);
+            }
+          } else {
+            pk[k >> 5][k & 31] = drop_pair(k, pack2<BF16>(p0, p1));
+          }
+        };
         // two branch-free copies of the loop (full tile / masked tile) so that the
         // scheduler can overlap the exponentials of many iterations
         if (full) {
@@ -571,7 +614,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
             const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
             acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
-            pk[k >> 5][k & 31] = drop_pair(k, pack2<BF16>(p0, p1));
+            emit(k, p0, p1);
           }
         } else {
 #pragma unroll
@@ -581,7 +624,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float p0 = 2 * k < vis ? ex2_approx(t0) : 0.f;
             const float p1 = 2 * k + 1 < vis ? ex2_approx(t1) : 0.f;
             acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
-            pk[k >> 5][k & 31] = drop_pair(k, pack2<BF16>(p0, p1));
+            emit(k, p0, p1);
           }
         }
         float ls;
@@ -614,9 +657,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         l_run = l_run * alpha + ls;
         m_run = m_new;
 
-        // P overwrites the first 64 columns of this tile's S region (the A operand of PV)
+        // P overwrites the first 64 (E4M3: 32) columns of this tile's S region (the A
+        // operand of PV)
         tmem_st32(tS, pk[0]);
-        tmem_st32(tS + 32, pk[1]);
+        if constexpr (!FP8) tmem_st32(tS + 32, pk[1]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -635,6 +679,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // O = O~ / l (with dropout O~ / (l (1 - p))), L = (m + log2 l) ln 2
           float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
           if constexpr (DROP) inv_l *= p.drop_rscale;
+          if constexpr (FP8) inv_l *= p.o_scale;
           uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
                           ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
 #pragma unroll
@@ -705,6 +750,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             float inv_l = l > 0.f ? 1.f / l : 0.f;
             if constexpr (DROP) inv_l *= p.drop_rscale;
+            if constexpr (FP8) inv_l *= p.o_scale;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
                             ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
 #pragma unroll 1
@@ -805,10 +851,38 @@ int make_map(CUtensorMap* m, const void* base, int d, int N, int BH, bool bf16) 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_TENSOR_MAP;
 }
 
+// E4M3 tensors as bytes. [BH, N, d]: boxes of 128 bytes (one row) x 128 rows x 1 head.
+int make_map_u8(CUtensorMap* m, const void* base, int d, int N, int BH) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return FA_ERR_TENSOR_MAP;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)N * d};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_TENSOR_MAP;
+}
+
+// V^T as bytes, [BH, d, ldvt] with ldvt a multiple of 16: boxes of 128 keys x d rows.
+int make_map_vt(CUtensorMap* m, const void* base, int d, int ldvt, int BH) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return FA_ERR_TENSOR_MAP;
+  cuuint64_t dims[3] = {(cuuint64_t)ldvt, (cuuint64_t)d, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)ldvt, (cuuint64_t)ldvt * d};
+  cuuint32_t box[3] = {128, (cuuint32_t)d, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_TENSOR_MAP;
+}
+
 struct DeviceInfo {
   int sms = 0;
   bool ok = false;
-  bool attr_set[2][2][2][2] = {};
+  bool attr_set[2][2][2][2][2] = {};
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -833,14 +907,14 @@ int device_info(DeviceInfo** out) {
   return FA_OK;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool DROP>
+template <int D, bool BF16, bool CAUSAL, bool DROP, bool FP8 = false>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
            DeviceInfo* di, int grid, cudaStream_t st) {
-  using LY = Layout<D>;
-  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, DROP>;
+  using LY = Layout<D, FP8 ? 1 : 2>;
+  auto kern = fa_fwd_kernel<D, BF16, CAUSAL, DROP, FP8>;
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    bool& set = di->attr_set[D == 128][BF16][CAUSAL][DROP];
+    bool& set = di->attr_set[D == 128][BF16][CAUSAL][DROP][FP8];
     if (!set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) !=
           cudaSuccess)
@@ -966,6 +1040,7 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
     grid = w.G;
   }
 
+  p.o_scale = 1.f;
   p.drop_bias = 0;
   p.drop_offset = 0;
   p.drop_rscale = 1.f;
@@ -1010,6 +1085,111 @@ __global__ void fa_dropout_mask_kernel(uint8_t* keep, long long rows, int Nq, in
       const int j = 16 * g + 4 * m + e;
       if (j < Nk) dst[j] = (uint8_t)flag[e];
     }
+  }
+}
+
+// ------------------------------------------------------------------------ E4M3 inputs
+// V [BH, Nk, d] -> V^T [BH, d, ldvt] (bytes), keys Nk..ldvt-1 zero. One block per
+// (head, 64 keys): 64 rows of d = 128 bytes are staged in shared memory, then written out
+// as 16-byte runs of consecutive keys.
+constexpr int VT_KEYS = 64;
+constexpr int VT_STRIDE = 144;  // staged row stride: 16-byte aligned, spreads the banks
+__global__ void __launch_bounds__(256) fa_fp8_transpose_v_kernel(const uint8_t* V, uint8_t* Vt,
+                                                                 int Nk, int ldvt) {
+  constexpr int D = 128;
+  __shared__ __align__(16) uint8_t tile[VT_KEYS * VT_STRIDE];
+  const int bh = blockIdx.x;
+  const int k0 = blockIdx.y * VT_KEYS;
+  const uint8_t* src = V + (size_t)bh * Nk * D;
+  uint8_t* dst = Vt + (size_t)bh * D * ldvt;
+  for (int idx = threadIdx.x; idx < VT_KEYS * (D / 16); idx += blockDim.x) {
+    const int row = idx / (D / 16), c16 = idx % (D / 16);
+    const int key = k0 + row;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (key < Nk) v = *reinterpret_cast<const uint4*>(src + (size_t)key * D + c16 * 16);
+    *reinterpret_cast<uint4*>(tile + row * VT_STRIDE + c16 * 16) = v;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < D * (VT_KEYS / 16); idx += blockDim.x) {
+    const int dcol = idx / (VT_KEYS / 16), kq = idx % (VT_KEYS / 16);
+    const int key = k0 + kq * 16;
+    if (key >= ldvt) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x |= (uint32_t)tile[(kq * 16 + 4 * q + e) * VT_STRIDE + dcol] << (8 * e);
+      w[q] = x;
+    }
+    *reinterpret_cast<uint4*>(dst + (size_t)dcol * ldvt + key) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+long long fp8_ldvt(int Nk) { return ((long long)Nk + 15) / 16 * 16; }
+size_t fp8_ws_bytes(long long BH, int Nk, int d) {
+  return (size_t)(BH * d * fp8_ldvt(Nk) + 255) / 256 * 256;
+}
+
+int run_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq,
+            int Nk, int d, float scale, int causal, float q_descale, float k_descale,
+            float v_descale, fa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+            void* stream) {
+  bool noop = false;
+  int rc = check_args(Q, K, V, O, L, B, H, Nq, Nk, d, scale, out_dtype, &noop);
+  if (rc != FA_OK || noop) return rc;
+  if (d != 128) return FA_ERR_HEAD_DIM;
+  for (float x : {q_descale, k_descale, v_descale})
+    if (!(x > 0.f) || !isfinite(x)) return FA_ERR_SCALE;
+  const long long BH = (long long)B * H;
+  if (!workspace || workspace_bytes < fp8_ws_bytes(BH, Nk, d)) return FA_ERR_WORKSPACE;
+  if ((uintptr_t)workspace & 15) return FA_ERR_ALIGN;
+  const double c = (double)scale * q_descale * k_descale * 1.4426950408889634;
+  if (!(c < 3.0e38)) return FA_ERR_SCALE;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != FA_OK) return rc;
+  const int ldvt = (int)fp8_ldvt(Nk);
+
+  Params p;
+  p.O = O;
+  p.L = L;
+  p.BH = (int)BH;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qblk = (int)(((long long)Nq + 2 * BM - 1) / (2 * BM));
+  p.n_items = (int)(p.n_qblk * BH);
+  p.n_kv_all = (Nk + BN - 1) / BN;
+  p.c = (float)c;
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.streamk = 0;
+  p.ws_part = nullptr;
+  p.ws_cnt = nullptr;
+  p.o_scale = v_descale;
+  p.drop_bias = 0;
+  p.drop_offset = 0;
+  p.drop_rscale = 1.f;
+  p.drop_keys = philox_keys(0);
+  const int grid = p.n_items < di->sms ? p.n_items : di->sms;
+
+  CUtensorMap mq, mk, mv;
+  if ((rc = make_map_u8(&mq, Q, d, Nq, (int)BH)) != FA_OK) return rc;
+  if ((rc = make_map_u8(&mk, K, d, Nk, (int)BH)) != FA_OK) return rc;
+  if ((rc = make_map_vt(&mv, workspace, d, ldvt, (int)BH)) != FA_OK) return rc;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const long long kblocks = (ldvt + VT_KEYS - 1) / VT_KEYS;
+  if (kblocks > 65535) return FA_ERR_SHAPE;
+  const dim3 tgrid((unsigned)BH, (unsigned)kblocks);
+  fa_fp8_transpose_v_kernel<<<tgrid, 256, 0, st>>>(reinterpret_cast<const uint8_t*>(V),
+                                                    reinterpret_cast<uint8_t*>(workspace), Nk, ldvt);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
+  const int key = (out_dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch<128, false, false, false, true>(mq, mk, mv, p, di, grid, st);
+    case 1: return launch<128, false, true, false, true>(mq, mk, mv, p, di, grid, st);
+    case 2: return launch<128, true, false, false, true>(mq, mk, mv, p, di, grid, st);
+    default: return launch<128, true, true, false, true>(mq, mk, mv, p, di, grid, st);
   }
 }
 
@@ -1126,6 +1306,19 @@ int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* 
     return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, nullptr, 0, false, stream);
   const DropArgs da{t, seed, offset};
   return run(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, nullptr, 0, false, stream, &da);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int Nk, int d) {
+  if (B <= 0 || H <= 0 || Nk <= 0 || d != 128) return 0;
+  return fp8_ws_bytes((long long)B * H, Nk, d);
+}
+
+int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+               int Nq, int Nk, int d, float scale, int causal, float q_descale, float k_descale,
+               float v_descale, fa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  return run_fp8(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, q_descale, k_descale, v_descale,
+                 out_dtype, workspace, workspace_bytes, stream);
 }
 
 int fa_dropout_mask(unsigned char* keep, int B, int H, int Nq, int Nk, float p_drop,

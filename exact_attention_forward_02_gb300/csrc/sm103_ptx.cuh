@@ -1,6 +1,6 @@
 // sm103_ptx.cuh -- thin inline-PTX wrappers for the Blackwell (sm_103a) features the
 // attention kernel uses: mbarriers, TMA tiled loads, Tensor Memory (tcgen05.alloc/ld/st),
-// the 5th-generation tensor-core MMA (tcgen05.mma, kind::f16) and its commit.
+// the 5th-generation tensor-core MMA (tcgen05.mma, kind::f16 and kind::f8f6f4) and its commit.
 //
 // Every wrapper maps to one documented PTX instruction (PTX ISA 8.7+ / 9.0).
 #pragma once
@@ -200,6 +200,28 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same two forms for 8-bit inputs (kind::f8f6f4; A and B both E4M3 here, whose type
+// code 0 in the instruction descriptor is the one umma_idesc_f16(0, ...) writes).
+// K per instruction is 32 elements (32 bytes), as for kind::f16 (16 elements, 32 bytes).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // arrive once on `bar` when every tcgen05 async op issued so far by this thread completes
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -293,6 +315,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   } else {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   }
+  return r;
+}
+
+// four fp32 values -> four E4M3 bytes (round to nearest even, saturating to +-448), the
+// first value in the lowest byte
+__device__ __forceinline__ uint32_t pack4_e4m3(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
   return r;
 }
 

@@ -14,6 +14,9 @@ Recipe (the pages benchmark only random-normal inputs, e.g. the CS336
   round-to-nearest-even to the workload's 16-bit type (fp16 or bf16);
 * the 16-bit values are the inputs of BOTH the CUDA path and the oracle (the
   oracle widens them exactly to float64).
+* FP8 workloads (dtype "e4m3") draw the same normals and round them to the OCP
+  FP8 E4M3 format (torch.float8_e4m3fn, round-to-nearest-even; |x| <= 448 for
+  every draw used here); their output O is bf16.
 """
 from __future__ import annotations
 
@@ -25,8 +28,10 @@ import torch
 
 F16 = "f16"
 BF16 = "bf16"
+FP8 = "e4m3"
 
-_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
+_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, FP8: torch.float8_e4m3fn}
+_ELEM_BYTES = {F16: 2, BF16: 2, FP8: 1}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -53,11 +58,16 @@ class Workload:
         return f / 2 if self.causal else f
 
     @property
+    def out_dtype(self) -> str:
+        """Type of O: the input type, or bf16 for FP8 inputs."""
+        return BF16 if self.dtype == FP8 else self.dtype
+
+    @property
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes: read Q, K, V once; write O (16-bit) and L (fp32)."""
-        e = 2
+        e = _ELEM_BYTES[self.dtype]
         bh = self.B * self.H
-        return bh * (self.Nq * self.d * e * 2 + self.Nk * self.d * e * 2 + self.Nq * 4)
+        return bh * (self.Nq * self.d * (e + 2) + self.Nk * self.d * e * 2 + self.Nq * 4)
 
     def describe(self) -> str:
         return (f"B={self.B},H={self.H},Nq={self.Nq},Nk={self.Nk},d={self.d},"
@@ -75,6 +85,12 @@ WORKLOADS = {
     "b4h12_q1000_k4097_d64_cross": Workload("b4h12_q1000_k4097_d64_cross", 4, 12, 1000, 4097, 64, F16, False, 1.0, 5),
 }
 
+# FP8 (E4M3) versions of the two d=128 benchmark workloads: same sizes, seeds and draws.
+FP8_WORKLOADS = {
+    "b2h8_n4096_d128_full_fp8": Workload("b2h8_n4096_d128_full_fp8", 2, 8, 4096, 4096, 128, FP8, False, 1.0, 2),
+    "b2h8_n8192_d128_causal_fp8": Workload("b2h8_n8192_d128_causal_fp8", 2, 8, 8192, 8192, 128, FP8, True, 1.0, 3),
+}
+
 
 def _draw(seed: int, tensor_id: int, shape, std: float, dtype: str) -> torch.Tensor:
     rng = np.random.default_rng([int(seed), int(tensor_id)])
@@ -85,6 +101,8 @@ def _draw(seed: int, tensor_id: int, shape, std: float, dtype: str) -> torch.Ten
     # double rounding at exact ties, which cannot matter for random normals;
     # avoid it anyway by rounding directly from float64 in torch.
     t = torch.from_numpy(x)
+    if dtype == FP8:  # torch rounds to E4M3 from float32; a float64 tie is measure-zero
+        t = t.to(torch.float32)
     return t.to(_TORCH_DTYPE[dtype])
 
 
@@ -106,5 +124,9 @@ def torch_dtype(dtype: str) -> torch.dtype:
 
 
 def to_f64_numpy(t: torch.Tensor) -> np.ndarray:
-    """Exact widening of a 16-bit tensor to a float64 numpy array."""
+    """Exact widening of a 16-bit or FP8 tensor to a float64 numpy array."""
     return t.to(torch.float64).numpy()
+
+
+def elem_bytes(dtype: str) -> int:
+    return _ELEM_BYTES[dtype]

@@ -150,6 +150,33 @@ int fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* 
                    fa_dtype dtype, float p_drop, unsigned long long seed, unsigned int offset,
                    void* stream);
 
+/* fa_fwd_fp8 -- the forward pass on FP8 inputs (E4M3, the OCP 8-bit format with 4 exponent
+ * and 3 mantissa bits, no infinities, |x| <= 448) with per-tensor descale factors, the
+ * FP8 attention of FlashAttention-3 that the "手写 Flash Attention" page names in its
+ * sections 6.1 and 7 (the pages give no further definition; this is the library's):
+ *     O = v_descale * softmax(scale * q_descale * k_descale * Q K^T [+causal]) V
+ *     L = ln sum_j exp(scale * q_descale * k_descale * <Q_i, K_j>)
+ * with Q, K, V decoded exactly from E4M3. Products accumulate in fp32; the probabilities
+ * fed to the second product are rounded to E4M3 (round to nearest even, as FlashAttention-3
+ * does), relative to the running row maximum; O is written as `out_dtype` (FA_BF16 or FA_F16).
+ * Arguments (DEVICE pointers, 16-byte aligned, dense row-major):
+ *   Q [B, H, Nq, d], K and V [B, H, Nk, d]   E4M3 bytes; d must be 128
+ *   O [B, H, Nq, d] out_dtype;  L [B, H, Nq] fp32 (natural log)
+ *   q_descale, k_descale, v_descale  finite and > 0 (1 when the inputs are unscaled)
+ *   workspace  at least fa_fwd_fp8_workspace_bytes(B, H, Nk, d) bytes, 16-byte aligned, no
+ *              initialisation: it receives V^T ([B, H, d, Nk rounded up to 16], keys
+ *              contiguous), which a first kernel writes and the attention kernel reads as
+ *              its K-major operand
+ * scale, causal and stream as in fa_fwd. Two kernels are queued on `stream`.
+ * Errors as fa_fwd (FA_ERR_DTYPE for an out_dtype other than FA_F16/FA_BF16, FA_ERR_HEAD_DIM
+ * for d != 128, FA_ERR_SCALE for a bad descale), plus FA_ERR_WORKSPACE for a missing or
+ * small workspace. */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int Nk, int d);
+int fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* L,
+               int B, int H, int Nq, int Nk, int d, float scale, int causal,
+               float q_descale, float k_descale, float v_descale, fa_dtype out_dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
 /* fa_dropout_mask -- write the keep mask that fa_fwd_dropout uses for these arguments:
  * keep [B, H, Nq, Nk] bytes (DEVICE pointer, caller-owned), 1 = kept, 0 = dropped.
  * Causality does not enter the mask (masked-out keys have P = 0 either way). One kernel
