@@ -12,17 +12,24 @@
 //   fa_bwd_dkv_kernel one 128-key tile per CTA, looping over query tiles: the transposed
 //                     products S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
 //                     dK += dS^T Q; TMEM: S^T | dP^T | dK | dV.
-// Roles per CTA (6 warps): warps 0-3 elementwise work (thread r owns TMEM lane r), warp 4
-// TMA producer, warp 5 MMA issuer (warp-converged, one elected lane issues).
+// Roles per CTA (10 warps): warps 0-7 elementwise work in two warpgroups that split the
+// tile's 128 columns in halves (thread r of either warpgroup owns TMEM lane r, warpgroup h
+// columns [64h, 64h + 64)), warp 8 TMA producer, warp 9 MMA issuer (warp-converged, one
+// elected lane issues). The 16-bit operands do not overwrite the scores of the next
+// product: dS has its own columns in the dQ kernel, and P^T, dS^T share S^T's columns in
+// the dK/dV kernel, so that the next tile's (dQ kernel: both, dK/dV kernel: dP^T) score
+// products run while the elementwise warps work.
 #pragma once
 
 namespace fa {
 
-constexpr int BW_WARPS = 6;
+constexpr int BW_EW_WARPS = 8;  // elementwise warps (two warpgroups)
+constexpr int BW_WARPS = BW_EW_WARPS + 2;
 constexpr int BW_THREADS = BW_WARPS * 32;
-constexpr int BW_WARP_LOAD = 4;
-constexpr int BW_WARP_MMA = 5;
+constexpr int BW_WARP_LOAD = 8;
+constexpr int BW_WARP_MMA = 9;
 constexpr int BW_MAX_SLOTS = 8;
+
 
 struct BwdParams {
   const void* O;      // dq kernel: forward output (16-bit), for D
@@ -42,9 +49,13 @@ struct BwdParams {
 
 struct BwdBars {
   uint64_t a_full, a_empty;            // the CTA's resident tiles (Q+dO, or K+V)
-  uint64_t full[BW_MAX_SLOTS];         // streamed tile pairs
+  uint64_t full[BW_MAX_SLOTS];         // streamed tile pairs (dQ kernel: K tiles)
   uint64_t release[BW_MAX_SLOTS];
+  uint64_t vfull[BW_MAX_SLOTS];        // dQ kernel: V tiles, a ring of their own
+  uint64_t vrelease[BW_MAX_SLOTS];
   uint64_t s_full;                      // both score products of the current tile in TMEM
+  uint64_t sdp_free;                    // the elementwise warps hold the scores in registers
+  uint64_t op_done;                     // the previous tile's accumulating products completed
   uint64_t p_full;                      // 16-bit operands written back to TMEM
   uint64_t done;                        // accumulators final for the current item
   uint64_t mma_drain;
@@ -70,6 +81,27 @@ struct BwdLayout {
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
 
+// dQ kernel: K and V stream through rings of their own, because V_j is read only by the
+// dP product and can leave long before K_j, which the dQ product still reads: a deeper
+// K ring then lets the next tiles' loads start early enough to hide their latency.
+template <int D>
+struct DqLayout {
+  static constexpr int TILE_BYTES = BM * D * 2;
+  static constexpr int CHUNK_BYTES = BM * 128;
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int FIXED = 2 * TILE_BYTES + 1024 + 1024;
+  static constexpr int V_SLOTS = 2;
+  static constexpr int K_FIT = (SMEM_LIMIT - FIXED - V_SLOTS * TILE_BYTES) / TILE_BYTES;
+  static constexpr int K_SLOTS = K_FIT > BW_MAX_SLOTS ? BW_MAX_SLOTS : K_FIT;
+  static constexpr int OFF_A = 0;                           // Q, dO (resident)
+  static constexpr int OFF_K = 2 * TILE_BYTES;              // K ring
+  static constexpr int OFF_V = OFF_K + K_SLOTS * TILE_BYTES;  // V ring
+  static constexpr int OFF_BAR = OFF_V + V_SLOTS * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(BwdBars) + 1024;
+  static_assert(K_SLOTS >= 3, "need three K slots");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+};
+
 // the r-th item of this CTA: boustrophedon deal (b, 2G-1-b, 2G+b, ...) of items sorted
 // by decreasing cost
 __device__ __forceinline__ int bw_item_of(int r) {
@@ -92,13 +124,16 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const BwdParams p) {
-  using LY = BwdLayout<D>;
-  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_COLS = 512;
+  using LY = DqLayout<D>;
+  // dS gets its own 64 columns, so that S and dP are free as soon as the elementwise warps
+  // have read them: the next tile's score products then overlap the elementwise pass
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384, T_COLS = 512;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + LY::OFF_BAR);
   const uint32_t sA = smem_u32(smem + LY::OFF_A);   // Q tile, then dO tile
-  const uint32_t sS = smem_u32(smem + LY::OFF_S);   // K_j, V_j pairs
+  const uint32_t sK = smem_u32(smem + LY::OFF_K);   // K ring
+  const uint32_t sV = smem_u32(smem + LY::OFF_V);   // V ring
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_kv_all = p.n_kt;
@@ -106,12 +141,18 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->a_full), 1);
     mbar_init(smem_u32(&bars->a_empty), 1);
-    for (int s = 0; s < LY::SLOTS; ++s) {
+    for (int s = 0; s < LY::K_SLOTS; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
       mbar_init(smem_u32(&bars->release[s]), 1);
     }
+    for (int s = 0; s < LY::V_SLOTS; ++s) {
+      mbar_init(smem_u32(&bars->vfull[s]), 1);
+      mbar_init(smem_u32(&bars->vrelease[s]), 1);
+    }
     mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->p_full), 4);
+    mbar_init(smem_u32(&bars->sdp_free), BW_EW_WARPS);
+    mbar_init(smem_u32(&bars->op_done), 1);
+    mbar_init(smem_u32(&bars->p_full), BW_EW_WARPS);  // one arrival per elementwise warp
     mbar_init(smem_u32(&bars->done), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     bars->abort_flag = 0;
@@ -143,7 +184,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     if (lane == 0) {
       uint32_t j_glob = 0, a_ph = 0;
       bool ok = true;
-      uint32_t issued = 0, last_par = 0;
+      uint32_t issued = 0, last_par = 0, vissued = 0, vlast_par = 0;
       bool a_issued = false;
       for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
         int bh, q0, n_kv;
@@ -160,27 +201,41 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         }
         a_issued = true;
         for (int j = 0; j < n_kv && ok; ++j, ++j_glob) {
-          const uint32_t slot = j_glob % LY::SLOTS, par = (j_glob / LY::SLOTS) & 1u;
-          if (j_glob >= (uint32_t)LY::SLOTS) {
-            const uint32_t u = j_glob - LY::SLOTS;  // the slot's previous tile pair
-            ok = wait_bar(smem_u32(&bars->release[u % LY::SLOTS]), (u / LY::SLOTS) & 1u, abort_flag, lim);
+          // K_j into K slot j_glob mod K_SLOTS, V_j into V slot j_glob mod V_SLOTS, each
+          // once the slot's previous tile has been released
+          const uint32_t ks = j_glob % LY::K_SLOTS, kpar = (j_glob / LY::K_SLOTS) & 1u;
+          if (j_glob >= (uint32_t)LY::K_SLOTS) {
+            const uint32_t u = j_glob - LY::K_SLOTS;
+            ok = wait_bar(smem_u32(&bars->release[u % LY::K_SLOTS]), (u / LY::K_SLOTS) & 1u, abort_flag, lim);
             if (!ok) break;
           }
-          const uint32_t f = smem_u32(&bars->full[slot]);
-          mbar_arrive_expect_tx(f, 2 * LY::TILE_BYTES);
-          const uint32_t dst = sS + slot * LY::PAIR_BYTES;
+          const uint32_t fk = smem_u32(&bars->full[ks]);
+          mbar_arrive_expect_tx(fk, LY::TILE_BYTES);
 #pragma unroll
-          for (int c = 0; c < LY::CHUNKS; ++c) {
-            tma_load_3d(dst + c * LY::CHUNK_BYTES, &tmK, f, c * 64, j * BN, bh);
-            tma_load_3d(dst + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, f, c * 64, j * BN, bh);
+          for (int c = 0; c < LY::CHUNKS; ++c)
+            tma_load_3d(sK + ks * LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmK, fk, c * 64, j * BN, bh);
+          issued |= 1u << ks;
+          last_par = (last_par & ~(1u << ks)) | (kpar << ks);
+          const uint32_t vs = j_glob % LY::V_SLOTS, vpar = (j_glob / LY::V_SLOTS) & 1u;
+          if (j_glob >= (uint32_t)LY::V_SLOTS) {
+            const uint32_t u = j_glob - LY::V_SLOTS;
+            ok = wait_bar(smem_u32(&bars->vrelease[u % LY::V_SLOTS]), (u / LY::V_SLOTS) & 1u, abort_flag, lim);
+            if (!ok) break;
           }
-          issued |= 1u << slot;
-          last_par = (last_par & ~(1u << slot)) | (par << slot);
+          const uint32_t fv = smem_u32(&bars->vfull[vs]);
+          mbar_arrive_expect_tx(fv, LY::TILE_BYTES);
+#pragma unroll
+          for (int c = 0; c < LY::CHUNKS; ++c)
+            tma_load_3d(sV + vs * LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, fv, c * 64, j * BN, bh);
+          vissued |= 1u << vs;
+          vlast_par = (vlast_par & ~(1u << vs)) | (vpar << vs);
         }
       }
       if (!ok) {
-        for (int s = 0; s < LY::SLOTS; ++s)
+        for (int s = 0; s < LY::K_SLOTS; ++s)
           if (issued & (1u << s)) wait_drain(smem_u32(&bars->full[s]), (last_par >> s) & 1u, lim);
+        for (int s = 0; s < LY::V_SLOTS; ++s)
+          if (vissued & (1u << s)) wait_drain(smem_u32(&bars->vfull[s]), (vlast_par >> s) & 1u, lim);
         if (a_issued) wait_drain(smem_u32(&bars->a_full), a_ph ^ 1, lim);
       }
     }
@@ -188,18 +243,24 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     constexpr uint32_t ID_S = umma_idesc_f16(BF16 ? 1 : 0, 0, 0, BM, BN);  // S, dP: K-major x K-major
     constexpr uint32_t ID_Q = umma_idesc_f16(BF16 ? 1 : 0, 0, 1, BM, D);   // dQ: A in TMEM, K MN-major
     const uint64_t dA = umma_smem_desc(sA, 16, 1024);
-    const uint64_t dB = umma_smem_desc(sS, 16, 1024);
-    const uint64_t dBmn = umma_smem_desc(sS, LY::CHUNK_BYTES, 1024);
+    const uint64_t dKd = umma_smem_desc(sK, 16, 1024);
+    const uint64_t dVd = umma_smem_desc(sV, 16, 1024);
+    const uint64_t dBmn = umma_smem_desc(sK, LY::CHUNK_BYTES, 1024);
     uint32_t j_glob = 0, a_ph = 0, p_ph = 0;
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t par) {
       return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
     };
-    // S = Q K^T into T_S, dP = dO V^T into T_DP (K = D per product)
-    auto issue_scores = [&](uint32_t slot) {
+    auto kv_wait = [&](uint32_t g) {
+      return wait_all(smem_u32(&bars->full[g % LY::K_SLOTS]), (g / LY::K_SLOTS) & 1u) &&
+             wait_all(smem_u32(&bars->vfull[g % LY::V_SLOTS]), (g / LY::V_SLOTS) & 1u);
+    };
+    // S = Q K^T into T_S, dP = dO V^T into T_DP (K = D per product) for K/V load g; V_g
+    // has no reader after dP and leaves its slot then
+    auto issue_scores = [&](uint32_t g) {
       if (elect_one()) {
-        const uint64_t dk = dB + ((slot * LY::PAIR_BYTES) >> 4);
-        const uint64_t dv = dk + (LY::TILE_BYTES >> 4);
+        const uint64_t dk = dKd + (((g % LY::K_SLOTS) * LY::TILE_BYTES) >> 4);
+        const uint64_t dv = dVd + (((g % LY::V_SLOTS) * LY::TILE_BYTES) >> 4);
         const uint64_t ddo = dA + (LY::TILE_BYTES >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -212,51 +273,72 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           umma_ss(tmem + T_DP, ddo + off, dv + off, ID_S, ks > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&bars->s_full));
+        umma_commit(smem_u32(&bars->vrelease[g % LY::V_SLOTS]));
       }
       __syncwarp();
     };
-    for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
-      int bh, q0, n_kv;
-      item_tiles(t, bh, q0, n_kv);
-      (void)bh; (void)q0;
-      ok = wait_all(smem_u32(&bars->a_full), a_ph) &&
-           wait_all(smem_u32(&bars->full[j_glob % LY::SLOTS]), (j_glob / LY::SLOTS) & 1u);
-      if (!ok) break;
-      a_ph ^= 1;
-      tc_fence_after();
-      issue_scores(j_glob % LY::SLOTS);
-      for (int j = 0; j < n_kv; ++j) {
-        const uint32_t slot = (j_glob + j) % LY::SLOTS;
+    auto n_kv_of = [&](int t) {
+      int bh, q0, n;
+      item_tiles(t, bh, q0, n);
+      return n;
+    };
+    // The CTA's tiles in order (items, then key tiles), one tile of lookahead: the scores
+    // of tile g+1 are issued once the elementwise warps hold tile g's in registers, and
+    // dQ += dS_g K_g once they have written dS_g. g numbers the K/V slot loads.
+    uint32_t f_ph = 0;
+    int rr_ = 0, t = bw_item_of(0);
+    if (t < p.n_items) {
+      ok = wait_all(smem_u32(&bars->a_full), a_ph) && kv_wait(0);
+      if (ok) {
+        a_ph ^= 1;
+        tc_fence_after();
+        issue_scores(0);
+        if (n_kv_of(t) == 1 && elect_one()) umma_commit(smem_u32(&bars->a_empty));
+        __syncwarp();
+      }
+    }
+    for (; t < p.n_items && ok; t = bw_item_of(++rr_)) {
+      const int n_kv = n_kv_of(t);
+      const int t_next = bw_item_of(rr_ + 1);
+      for (int j = 0; j < n_kv; ++j, ++j_glob) {
+        const uint32_t slot = j_glob % LY::K_SLOTS;
+        const bool last_in_item = j + 1 == n_kv;
+        ok = wait_all(smem_u32(&bars->sdp_free), f_ph);
+        if (!ok) break;
+        f_ph ^= 1;
+        if (!last_in_item || t_next < p.n_items) {
+          if (last_in_item) {  // the next item's Q, dO
+            ok = wait_all(smem_u32(&bars->a_full), a_ph);
+            if (!ok) break;
+            a_ph ^= 1;
+          }
+          ok = kv_wait(j_glob + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(j_glob + 1);
+          // the scores of an item's last tile are the last reads of its Q, dO
+          const int j_next = last_in_item ? 0 : j + 1;
+          const int n_next = last_in_item ? n_kv_of(t_next) : n_kv;
+          if (j_next + 1 == n_next && elect_one()) umma_commit(smem_u32(&bars->a_empty));
+          __syncwarp();
+        }
         ok = wait_all(smem_u32(&bars->p_full), p_ph);
         if (!ok) break;
         p_ph ^= 1;
         tc_fence_after();
         // dQ += dS K_j : M=128 queries, N=D, K=128 keys; dS from TMEM, K_j MN-major
         if (elect_one()) {
-          const uint64_t dk = dBmn + ((slot * LY::PAIR_BYTES) >> 4);
+          const uint64_t dk = dBmn + ((slot * LY::TILE_BYTES) >> 4);
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
-            umma_ts(tmem + T_DQ, tmem + T_S + ks * 8, dk + ((ks * 16 * 128) >> 4), ID_Q,
+            umma_ts(tmem + T_DQ, tmem + T_DS + ks * 8, dk + ((ks * 16 * 128) >> 4), ID_Q,
                     (j > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&bars->op_done));
+          umma_commit(smem_u32(&bars->release[slot]));  // K_j: no further reader
+          if (last_in_item) umma_commit(smem_u32(&bars->done));
         }
-        __syncwarp();
-        if (j + 1 < n_kv) {
-          const uint32_t nslot = (j_glob + j + 1) % LY::SLOTS;
-          ok = wait_all(smem_u32(&bars->full[nslot]), ((j_glob + j + 1) / LY::SLOTS) & 1u);
-          if (!ok) break;
-          tc_fence_after();
-          issue_scores(nslot);
-        } else {
-          if (elect_one()) {
-            umma_commit(smem_u32(&bars->done));
-            umma_commit(smem_u32(&bars->a_empty));
-          }
-          __syncwarp();
-        }
-        if (elect_one()) umma_commit(smem_u32(&bars->release[(j_glob + j) % LY::SLOTS]));
         __syncwarp();
       }
-      j_glob += n_kv;
     }
     if (elect_one()) umma_commit(smem_u32(&bars->mma_drain));
     __syncwarp();
@@ -265,10 +347,14 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   } else {
     // ------------------------------------------------------------------- elementwise
     const int wq = warp & 3;
+    const int hf = warp >> 2;  // column half: keys [64 hf, 64 hf + 64) of every key tile
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP, tQ = tmem + lane_off + T_DQ;
-    uint32_t s_ph = 0, d_ph = 0;
+    const uint32_t tS = tmem + lane_off + T_S + hf * 64, tDP = tmem + lane_off + T_DP + hf * 64;
+    const uint32_t tDS = tmem + lane_off + T_DS + hf * 32;
+    const uint32_t tQ = tmem + lane_off + T_DQ;
+    uint32_t s_ph = 0, d_ph = 0, o_ph = 0;
+    bool first_tile = true;
     bool ok = true;
     for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, q0, n_kv;
@@ -276,7 +362,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       const int row = q0 + r;
       const bool valid = row < p.Nq;
       const size_t grow = (size_t)bh * p.Nq + (valid ? row : 0);
-      // D = rowsum(dO o O) in fp32 from the 16-bit rows
+      // D = rowsum(dO o O) in fp32 from the 16-bit rows (both halves compute it; the
+      // second read of the row hits L2); half 0 stores it for the dK/dV kernel
       float Drow = 0.f, L2 = INFINITY;
       if (valid) {
         const uint4* o4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.O) + grow * D * 2);
@@ -295,7 +382,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           }
         }
         Drow = acc2[0] + acc2[1];
-        p.Dws[grow] = Drow;
+        if (hf == 0) p.Dws[grow] = Drow;
         L2 = p.L[grow] * 1.4426950408889634f;
       }
       const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;
@@ -305,43 +392,74 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         s_ph ^= 1;
         tc_fence_after();
         const int vis = kv_lim - j * BN;
-        // two halves of 64 keys: P = exp2(S c - L log2 e), dS = P (dP - D) -> 16-bit over S
+        // this half's 64 keys: P = exp2(S c - L log2 e), dS = P (dP - D) -> 16-bit pairs
+        // over the first 32 columns of the half
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(tS, sr[0]);
+        tmem_ld32(tS + 32, sr[1]);
+        tmem_ld32(tDP, dr[0]);
+        tmem_ld32(tDP + 32, dr[1]);
+        tmem_wait_ld();
+        reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
+        // S and dP are in registers: their columns may take the next tile's scores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->sdp_free));
+        // in phases over all 64 values (exponent arguments, exponentials, products), so
+        // that the exponentials issue back to back instead of one dependent chain per pair
+        const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-L2, -L2), nd2 = f2(-Drow, -Drow);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sr[2][32], dr[2][32];
-          tmem_ld32(tS + h * 64, sr[0]);
-          tmem_ld32(tS + h * 64 + 32, sr[1]);
-          tmem_ld32(tDP + h * 64, dr[0]);
-          tmem_ld32(tDP + h * 64 + 32, dr[1]);
-          tmem_wait_ld();
-          reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
-          uint32_t pk[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int key0 = h * 64 + 2 * k;
-            const float s0 = __uint_as_float(sr[k >> 4][(2 * k) & 31]);
-            const float s1 = __uint_as_float(sr[k >> 4][(2 * k + 1) & 31]);
-            const float g0 = __uint_as_float(dr[k >> 4][(2 * k) & 31]);
-            const float g1 = __uint_as_float(dr[k >> 4][(2 * k + 1) & 31]);
-            const float p0 = key0 < vis ? ex2_approx(fmaf(s0, p.c, -L2)) : 0.f;
-            const float p1 = key0 + 1 < vis ? ex2_approx(fmaf(s1, p.c, -L2)) : 0.f;
-            pk[k] = pack2<BF16>(p0 * (g0 - Drow), p1 * (g1 - Drow));
-          }
-          tmem_st32(tS + h * 32, pk);
+        for (int k = 0; k < 32; ++k) {
+          float t0, t1;
+          f2_split(f2_fma(f2(__uint_as_float(sr[k >> 4][(2 * k) & 31]),
+                             __uint_as_float(sr[k >> 4][(2 * k + 1) & 31])), c2, nl2), t0, t1);
+          sr[k >> 4][(2 * k) & 31] = __float_as_uint(t0);
+          sr[k >> 4][(2 * k + 1) & 31] = __float_as_uint(t1);
         }
+        if (vis >= hf * 64 + 64) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            sr[e >> 5][e & 31] = __float_as_uint(ex2_approx(__uint_as_float(sr[e >> 5][e & 31])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            sr[e >> 5][e & 31] = __float_as_uint(
+                hf * 64 + e < vis ? ex2_approx(__uint_as_float(sr[e >> 5][e & 31])) : 0.f);
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          float a0, a1;
+          f2_split(f2_mul(f2(__uint_as_float(sr[k >> 4][(2 * k) & 31]),
+                             __uint_as_float(sr[k >> 4][(2 * k + 1) & 31])),
+                          f2_add(f2(__uint_as_float(dr[k >> 4][(2 * k) & 31]),
+                                    __uint_as_float(dr[k >> 4][(2 * k + 1) & 31])), nd2)),
+                   a0, a1);
+          pk[k] = pack2<BF16>(a0, a1);
+        }
+        // the previous tile's dQ product reads the dS columns until it completes
+        if (!first_tile) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->op_done), o_ph, abort_flag, lim));
+          if (!ok) break;
+          o_ph ^= 1;
+          tc_fence_after();
+        }
+        first_tile = false;
+        tmem_st32(tDS, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
       }
       if (!ok) break;
-      // dQ = scale * (dS K) -> 16-bit
+      // dQ = scale * (dS K) -> 16-bit; this half stores columns [D/2 hf, D/2 (hf + 1))
       ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->done), d_ph, abort_flag, lim));
       if (!ok) break;
       d_ph ^= 1;
       tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+      for (int qq = 0; qq < D / 64; ++qq) {
+        const int q = hf * (D / 64) + qq;
         uint32_t o[32];
         tmem_ld32(tQ + q * 32, o);
         tmem_wait_ld();
@@ -391,7 +509,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       mbar_init(smem_u32(&bars->release[s]), 1);
     }
     mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->p_full), 4);
+    mbar_init(smem_u32(&bars->sdp_free), BW_EW_WARPS);
+    mbar_init(smem_u32(&bars->op_done), 1);
+    mbar_init(smem_u32(&bars->p_full), BW_EW_WARPS);  // one arrival per elementwise warp
     mbar_init(smem_u32(&bars->done), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
     bars->abort_flag = 0;
@@ -477,25 +597,35 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     auto wait_all = [&](uint32_t bar, uint32_t par) {
       return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
     };
-    auto issue_scores = [&](uint32_t slot) {
+    // S^T = K Q_i^T into T_S, dP^T = V dO_i^T into T_DP (K = D per product)
+    auto issue_dpt = [&](uint32_t slot) {
+      if (elect_one()) {
+        const uint64_t ddo = dB + ((slot * LY::PAIR_BYTES) >> 4) + (LY::TILE_BYTES >> 4);
+        const uint64_t dv = dA + (LY::TILE_BYTES >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+          umma_ss(tmem + T_DP, dv + off, ddo + off, ID_S, ks > 0 ? 1u : 0u);  // V dO^T
+        }
+      }
+      __syncwarp();
+    };
+    auto issue_st = [&](uint32_t slot) {
       if (elect_one()) {
         const uint64_t dq = dB + ((slot * LY::PAIR_BYTES) >> 4);
-        const uint64_t ddo = dq + (LY::TILE_BYTES >> 4);
-        const uint64_t dv = dA + (LY::TILE_BYTES >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
           umma_ss(tmem + T_S, dA + off, dq + off, ID_S, ks > 0 ? 1u : 0u);   // K Q^T
         }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
-          umma_ss(tmem + T_DP, dv + off, ddo + off, ID_S, ks > 0 ? 1u : 0u); // V dO^T
-        }
         umma_commit(smem_u32(&bars->s_full));
       }
       __syncwarp();
     };
+    // Per query tile i: P^T and dS^T go back over S^T, so dP^T's columns are free once the
+    // elementwise warps have read them: dP^T(i+1) is issued during their pass over tile i,
+    // S^T(i+1) after dV(i) and dK(i), which read P^T(i) and dS^T(i).
+    uint32_t f_ph = 0;
     for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, k0, i0, n_q;
       item_tiles(t, bh, k0, i0, n_q);
@@ -505,9 +635,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       if (!ok) break;
       a_ph ^= 1;
       tc_fence_after();
-      issue_scores(i_glob % LY::SLOTS);
+      issue_dpt(i_glob % LY::SLOTS);
+      issue_st(i_glob % LY::SLOTS);
       for (int i = 0; i < n_q; ++i) {
         const uint32_t slot = (i_glob + i) % LY::SLOTS;
+        const uint32_t nslot = (i_glob + i + 1) % LY::SLOTS;
+        const bool has_next = i + 1 < n_q;
+        ok = wait_all(smem_u32(&bars->sdp_free), f_ph);
+        if (!ok) break;
+        f_ph ^= 1;
+        if (has_next) {
+          ok = wait_all(smem_u32(&bars->full[nslot]), ((i_glob + i + 1) / LY::SLOTS) & 1u);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dpt(nslot);
+        }
         ok = wait_all(smem_u32(&bars->p_full), p_ph);
         if (!ok) break;
         p_ph ^= 1;
@@ -522,26 +664,17 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           }
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks) {  // dK += dS^T Q_i
-            umma_ts(tmem + T_DK, tmem + T_DP + ks * 8, dq + ((ks * 16 * 128) >> 4), ID_G,
+            umma_ts(tmem + T_DK, tmem + T_S + 64 + ks * 8, dq + ((ks * 16 * 128) >> 4), ID_G,
                     (i > 0 || ks > 0) ? 1u : 0u);
           }
-        }
-        __syncwarp();
-        if (i + 1 < n_q) {
-          const uint32_t nslot = (i_glob + i + 1) % LY::SLOTS;
-          ok = wait_all(smem_u32(&bars->full[nslot]), ((i_glob + i + 1) / LY::SLOTS) & 1u);
-          if (!ok) break;
-          tc_fence_after();
-          issue_scores(nslot);
-        } else {
-          if (elect_one()) {
+          umma_commit(smem_u32(&bars->release[slot]));  // Q_i, dO_i: no further reader
+          if (!has_next) {
             umma_commit(smem_u32(&bars->done));
             umma_commit(smem_u32(&bars->a_empty));
           }
-          __syncwarp();
         }
-        if (elect_one()) umma_commit(smem_u32(&bars->release[(i_glob + i) % LY::SLOTS]));
         __syncwarp();
+        if (has_next) issue_st(nslot);
       }
       i_glob += n_q;
     }
@@ -552,9 +685,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   } else {
     // ------------------------------------------------------------------- elementwise
     const int wq = warp & 3;
+    const int hf = warp >> 2;         // column half: queries [64 hf, 64 hf + 64) of each tile
     const int r = wq * 32 + lane;     // key row of the tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP;
+    const uint32_t tS = tmem + lane_off + T_S + hf * 64, tDP = tmem + lane_off + T_DP + hf * 64;
+    // this half's 16-bit P^T at S^T columns [32 hf, 32 hf + 32), dS^T 64 columns further
+    const uint32_t tPT = tmem + lane_off + T_S + hf * 32;
     const uint32_t tK = tmem + lane_off + T_DK, tV = tmem + lane_off + T_DV;
     uint32_t s_ph = 0, d_ph = 0;
     bool ok = true;
@@ -564,56 +700,85 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       const int key = k0 + r;
       for (int i = 0; i < n_q; ++i) {
         const int q0 = (i0 + i) * BM;
-        // this query tile's L log2(e) and D, one value per thread (rows past Nq: L = +inf
-        // so that P = 0); the previous tile's readers finished at the barrier that ended
-        // its iteration
+        // this query tile's L log2(e) (staged by half 0) and D (by half 1), one value per
+        // thread (rows past Nq: L = +inf so that P = 0); the previous tile's readers
+        // finished at the barrier that ended its iteration
         {
           const int qrow = q0 + r;
           const bool qv = qrow < p.Nq;
           const size_t g = (size_t)bh * p.Nq + (qv ? qrow : 0);
-          sLD[r] = qv ? p.L[g] * 1.4426950408889634f : INFINITY;
-          sLD[128 + r] = qv ? p.Dws[g] : 0.f;
+          if (hf == 0)
+            sLD[r] = qv ? p.L[g] * 1.4426950408889634f : INFINITY;
+          else
+            sLD[128 + r] = qv ? p.Dws[g] : 0.f;
         }
-        // one barrier both publishes sLD and makes the wait's outcome the same in all four
-        // warps (so that a timeout ends the loop everywhere, never at a barrier)
-        ok = named_bar_red_and(2, 128, wait_bar(smem_u32(&bars->s_full), s_ph, abort_flag, lim));
+        // one barrier both publishes sLD and makes the wait's outcome the same in all
+        // elementwise warps (so that a timeout ends the loop everywhere, never at a barrier)
+        ok = named_bar_red_and(2, BW_EW_WARPS * 32,
+                               wait_bar(smem_u32(&bars->s_full), s_ph, abort_flag, lim));
         if (!ok) break;
         s_ph ^= 1;
         tc_fence_after();
         // causal: query q sees this key iff q >= key; first visible query of the tile:
         const int qfirst = CAUSAL ? key - q0 : 0;
+        uint32_t sr[2][32], dr[2][32];
+        tmem_ld32(tS, sr[0]);
+        tmem_ld32(tS + 32, sr[1]);
+        tmem_ld32(tDP, dr[0]);
+        tmem_ld32(tDP + 32, dr[1]);
+        tmem_wait_ld();
+        reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
+        // both halves hold their scores in registers: S^T may now take P^T and dS^T, and
+        // dP^T's columns the next tile's product
+        tc_fence_before();
+        named_bar_sync(3, BW_EW_WARPS * 32);
+        if (lane == 0) mbar_arrive(smem_u32(&bars->sdp_free));
+        // in phases over all 64 values (exponent arguments, exponentials, products), so
+        // that the exponentials issue back to back instead of one dependent chain per pair
+        const uint64_t c2 = f2(p.c, p.c);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sr[2][32], dr[2][32];
-          tmem_ld32(tS + h * 64, sr[0]);
-          tmem_ld32(tS + h * 64 + 32, sr[1]);
-          tmem_ld32(tDP + h * 64, dr[0]);
-          tmem_ld32(tDP + h * 64 + 32, dr[1]);
-          tmem_wait_ld();
-          reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
-          uint32_t pp[32], pd[32];
+        for (int k = 0; k < 32; ++k) {
+          const float2 l2 = *reinterpret_cast<const float2*>(sLD + hf * 64 + 2 * k);
+          float t0, t1;
+          f2_split(f2_fma(f2(__uint_as_float(sr[k >> 4][(2 * k) & 31]),
+                             __uint_as_float(sr[k >> 4][(2 * k + 1) & 31])), c2, f2(-l2.x, -l2.y)),
+                   t0, t1);
+          sr[k >> 4][(2 * k) & 31] = __float_as_uint(t0);
+          sr[k >> 4][(2 * k + 1) & 31] = __float_as_uint(t1);
+        }
+        if (qfirst <= hf * 64) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int qc = h * 64 + 2 * k;  // query column within the tile
-            const float2 l2 = *reinterpret_cast<const float2*>(sLD + qc);
-            const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + qc);
-            const float s0 = __uint_as_float(sr[k >> 4][(2 * k) & 31]);
-            const float s1 = __uint_as_float(sr[k >> 4][(2 * k + 1) & 31]);
-            const float g0 = __uint_as_float(dr[k >> 4][(2 * k) & 31]);
-            const float g1 = __uint_as_float(dr[k >> 4][(2 * k + 1) & 31]);
-            const float p0 = qc >= qfirst ? ex2_approx(fmaf(s0, p.c, -l2.x)) : 0.f;
-            const float p1 = qc + 1 >= qfirst ? ex2_approx(fmaf(s1, p.c, -l2.y)) : 0.f;
-            pp[k] = pack2<BF16>(p0, p1);
-            pd[k] = pack2<BF16>(p0 * (g0 - dd.x), p1 * (g1 - dd.y));
+          for (int e = 0; e < 64; ++e)
+            sr[e >> 5][e & 31] = __float_as_uint(ex2_approx(__uint_as_float(sr[e >> 5][e & 31])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            sr[e >> 5][e & 31] = __float_as_uint(
+                hf * 64 + e >= qfirst ? ex2_approx(__uint_as_float(sr[e >> 5][e & 31])) : 0.f);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pp[16], pd[16];
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + hf * 64 + c * 32 + 2 * kk);
+            const float p0 = __uint_as_float(sr[c][2 * kk]), p1 = __uint_as_float(sr[c][2 * kk + 1]);
+            float a0, a1;
+            f2_split(f2_mul(f2(p0, p1),
+                            f2_add(f2(__uint_as_float(dr[c][2 * kk]), __uint_as_float(dr[c][2 * kk + 1])),
+                                   f2(-dd.x, -dd.y))),
+                     a0, a1);
+            pp[kk] = pack2<BF16>(p0, p1);
+            pd[kk] = pack2<BF16>(a0, a1);
           }
-          tmem_st32(tS + h * 32, pp);
-          tmem_st32(tDP + h * 32, pd);
+          tmem_st16(tPT + c * 16, pp);
+          tmem_st16(tPT + 64 + c * 16, pd);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
-        named_bar_sync(2, 128);  // every thread is done reading sLD
+        named_bar_sync(2, BW_EW_WARPS * 32);  // every thread is done reading sLD
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->done), d_ph, abort_flag, lim));
@@ -622,8 +787,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       tc_fence_after();
       const bool valid = key < p.Nk;
       const size_t grow = (size_t)bh * p.Nk + (valid ? key : 0);
+      // this half stores columns [D/2 hf, D/2 (hf + 1)) of dK and dV
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+      for (int qq = 0; qq < D / 64; ++qq) {
+        const int q = hf * (D / 64) + qq;
         uint32_t o[32];
         uint32_t w16[16];
         tmem_ld32(tK + q * 32, o);

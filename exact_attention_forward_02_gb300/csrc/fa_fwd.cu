@@ -1198,6 +1198,7 @@ template <int D, bool BF16, bool CAUSAL>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const CUtensorMap& mdo, BwdParams p, DeviceInfo* di, cudaStream_t st) {
   using LY = BwdLayout<D>;
+  using LQ = DqLayout<D>;
   auto kq = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
   auto kkv = fa_bwd_dkv_kernel<D, BF16, CAUSAL>;
   static bool attr_set[kMaxDevices] = {};
@@ -1206,7 +1207,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) != cudaSuccess ||
+      if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM_BYTES) != cudaSuccess)
         return FA_ERR_CUDA;
       attr_set[dev] = true;
@@ -1215,7 +1216,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   // query tiles first: D (needed by the second kernel) and dQ
   p.n_items = p.BH * p.n_qt;
   int grid = p.n_items < di->sms ? p.n_items : di->sms;
-  kq<<<grid, BW_THREADS, LY::SMEM_BYTES, st>>>(mq, mdo, mk, mv, p);
+  kq<<<grid, BW_THREADS, LQ::SMEM_BYTES, st>>>(mq, mdo, mk, mv, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
   p.n_items = p.BH * p.n_kt;
