@@ -182,6 +182,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == BW_WARP_LOAD) {
     if (lane == 0) {
+      // streamed tiles are read by every CTA working on the same head: keep them in L2;
+      // the CTA's resident tiles are read once
+      const uint64_t pol_reuse = l2_policy_evict_last();
+      const uint64_t pol_once = l2_policy_evict_first();
       uint32_t j_glob = 0, a_ph = 0;
       bool ok = true;
       uint32_t issued = 0, last_par = 0, vissued = 0, vlast_par = 0;
@@ -196,8 +200,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_arrive_expect_tx(af, 2 * LY::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < LY::CHUNKS; ++c) {
-          tma_load_3d(sA + c * LY::CHUNK_BYTES, &tmQ, af, c * 64, q0, bh);
-          tma_load_3d(sA + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmdO, af, c * 64, q0, bh);
+          tma_load_3d_hint(sA + c * LY::CHUNK_BYTES, &tmQ, af, c * 64, q0, bh, pol_once);
+          tma_load_3d_hint(sA + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmdO, af, c * 64, q0, bh, pol_once);
         }
         a_issued = true;
         for (int j = 0; j < n_kv && ok; ++j, ++j_glob) {
@@ -213,7 +217,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           mbar_arrive_expect_tx(fk, LY::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < LY::CHUNKS; ++c)
-            tma_load_3d(sK + ks * LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmK, fk, c * 64, j * BN, bh);
+            tma_load_3d_hint(sK + ks * LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmK, fk, c * 64, j * BN, bh,
+                             pol_reuse);
           issued |= 1u << ks;
           last_par = (last_par & ~(1u << ks)) | (kpar << ks);
           const uint32_t vs = j_glob % LY::V_SLOTS, vpar = (j_glob / LY::V_SLOTS) & 1u;
@@ -226,7 +231,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           mbar_arrive_expect_tx(fv, LY::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < LY::CHUNKS; ++c)
-            tma_load_3d(sV + vs * LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, fv, c * 64, j * BN, bh);
+            tma_load_3d_hint(sV + vs * LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, fv, c * 64, j * BN, bh,
+                             pol_reuse);
           vissued |= 1u << vs;
           vlast_par = (vlast_par & ~(1u << vs)) | (vpar << vs);
         }
@@ -543,6 +549,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == BW_WARP_LOAD) {
     if (lane == 0) {
+      // streamed tiles are read by every CTA working on the same head: keep them in L2;
+      // the CTA's resident tiles are read once
+      const uint64_t pol_reuse = l2_policy_evict_last();
+      const uint64_t pol_once = l2_policy_evict_first();
       uint32_t i_glob = 0, a_ph = 0;
       bool ok = true;
       uint32_t issued = 0, last_par = 0;
@@ -557,8 +567,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         mbar_arrive_expect_tx(af, 2 * LY::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < LY::CHUNKS; ++c) {
-          tma_load_3d(sA + c * LY::CHUNK_BYTES, &tmK, af, c * 64, k0, bh);
-          tma_load_3d(sA + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, af, c * 64, k0, bh);
+          tma_load_3d_hint(sA + c * LY::CHUNK_BYTES, &tmK, af, c * 64, k0, bh, pol_once);
+          tma_load_3d_hint(sA + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmV, af, c * 64, k0, bh, pol_once);
         }
         a_issued = true;
         for (int i = 0; i < n_q && ok; ++i, ++i_glob) {
@@ -573,8 +583,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           const uint32_t dst = sS + slot * LY::PAIR_BYTES;
 #pragma unroll
           for (int c = 0; c < LY::CHUNKS; ++c) {
-            tma_load_3d(dst + c * LY::CHUNK_BYTES, &tmQ, f, c * 64, (i0 + i) * BM, bh);
-            tma_load_3d(dst + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmdO, f, c * 64, (i0 + i) * BM, bh);
+            tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, &tmQ, f, c * 64, (i0 + i) * BM, bh, pol_reuse);
+            tma_load_3d_hint(dst + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmdO, f, c * 64, (i0 + i) * BM, bh,
+                             pol_reuse);
           }
           issued |= 1u << slot;
           last_par = (last_par & ~(1u << slot)) | (par << slot);
