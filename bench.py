@@ -390,8 +390,13 @@ def run_bwd(args):
         O = torch.empty_like(q)
         L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
         dt = fa.FA_BF16 if w.dtype == gen.BF16 else fa.FA_F16
-        rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(),
-                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt, sp)
+        if args.dropout > 0:  # the forward whose mask the backward regenerates
+            rc = fa.fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(),
+                                   L.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt,
+                                   args.dropout, 1234, 1, sp)
+        else:
+            rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(),
+                           w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt, sp)
         if rc != 0:
             raise fa.FAError(rc)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -402,9 +407,15 @@ def run_bwd(args):
 
     def launch(w):
         q, k, v, O, do, L, dq, dk, dv, ws, dt = bufs[w.name]
-        rc = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), do.data_ptr(),
-                       L.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.Nq,
-                       w.Nk, w.d, w.scale, w.causal, dt, ws.data_ptr(), ws.numel(), sp)
+        if args.dropout > 0:
+            rc = fa.fa_bwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(),
+                                   do.data_ptr(), L.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, dt,
+                                   args.dropout, 1234, 1, ws.data_ptr(), ws.numel(), sp)
+        else:
+            rc = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), do.data_ptr(),
+                           L.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H,
+                           w.Nq, w.Nk, w.d, w.scale, w.causal, dt, ws.data_ptr(), ws.numel(), sp)
         if rc != 0:
             raise fa.FAError(rc)
 
@@ -442,7 +453,9 @@ def run_bwd(args):
         "dtype": "+".join(sorted({w.dtype for w in wl})), "data": "synthetic",
         "config": {"workload": "+".join(names), "shapes": [w.describe() for w in wl],
                    "l2": "flushed before every call (256 MiB write, outside the events)",
-                   "flops": "10*B*H*Nq*Nk*d, halved when causal"},
+                   "flops": "10*B*H*Nq*Nk*d, halved when causal",
+                   "entry_point": "fa_bwd_dropout" if args.dropout > 0 else "fa_bwd",
+                   "dropout": args.dropout},
         "breakdown": {w.name: {"ms": round(statistics.fmean(per[w.name]), 5),
                                "tflops": round(flops[w.name] / (statistics.fmean(per[w.name]) * 1e-3) / 1e12, 1),
                                "pct_of_peak": round(100 * flops[w.name] / (statistics.fmean(per[w.name]) * 1e-3) / 1e12 / peak, 1)}

@@ -68,6 +68,10 @@ def _load() -> ctypes.CDLL:
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd.argtypes = [vp] * 9 + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd_dropout.restype = ctypes.c_int
+    lib.fa_bwd_dropout.argtypes = [vp] * 9 + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
+        ctypes.c_uint, vp, ctypes.c_size_t, vp]
     lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
     lib.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
@@ -150,6 +154,15 @@ def fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, causal, dtype,
     return int(lib.fa_bwd(Q, K, V, O, dO, L, dQ, dK, dV, int(B), int(H), int(Nq), int(Nk), int(d),
                           float(scale), int(bool(causal)), int(dtype), workspace,
                           int(workspace_bytes), stream))
+
+
+def fa_bwd_dropout(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, causal, dtype, p_drop,
+                   seed, offset, workspace, workspace_bytes, stream) -> int:
+    """C-ABI call of the backward pass of fa_fwd_dropout (same p_drop, seed, offset)."""
+    return int(lib.fa_bwd_dropout(Q, K, V, O, dO, L, dQ, dK, dV, int(B), int(H), int(Nq), int(Nk),
+                                  int(d), float(scale), int(bool(causal)), int(dtype),
+                                  float(p_drop), int(seed), int(offset), workspace,
+                                  int(workspace_bytes), stream))
 
 
 def fa_bwd_workspace_bytes(B, H, Nq, Nk, d) -> int:

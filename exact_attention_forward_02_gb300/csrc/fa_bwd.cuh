@@ -45,6 +45,11 @@ struct BwdParams {
   float c;            // scale * log2(e)
   float scale;
   unsigned long long wait_limit_ns;
+  // dropout (kernels instantiated with DROP): the mask of the forward's (seed, offset)
+  uint32_t drop_bias;     // (0x100 - t) * 0x00010001 for the 8-bit threshold t
+  uint32_t drop_offset;
+  float drop_rscale;      // 256 / (256 - t)
+  PhiloxKeys drop_keys;
 };
 
 struct BwdBars {
@@ -119,7 +124,7 @@ __device__ __forceinline__ void store_row16(void* base, size_t row, int d_cols, 
 // ============================================================================ dQ kernel
 // CTA item: (bh, query tile qt). Streams K_j, V_j; per key tile:
 //   S = Q K_j^T, dP = dO V_j^T  (TMEM)  ->  dS = P o (dP - D)  (16-bit, over S)  ->  dQ += dS K_j
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -393,6 +398,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       }
       const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;
       for (int j = 0; j < n_kv; ++j) {
+        // dropout ("Algorithm 4": dP = dP_dropped o Z): this row's keep bits for the half's
+        // 64 keys, drawn before the scores are ready
+        uint32_t kb[2] = {0, 0};
+        if constexpr (DROP)
+          dropout_row_bits<2>((uint32_t)(j * (BN / 16) + hf * 4), (uint32_t)row, (uint32_t)bh,
+                              p.drop_offset, p.drop_keys, p.drop_bias, kb);
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), s_ph, abort_flag, lim));
         if (!ok) break;
         s_ph ^= 1;
@@ -435,11 +446,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
+          const uint64_t g2 = f2(__uint_as_float(dr[k >> 4][(2 * k) & 31]),
+                                 __uint_as_float(dr[k >> 4][(2 * k + 1) & 31]));
+          uint64_t gd;  // dP - D, with dP = dP_dropped * Z under dropout
+          if constexpr (DROP) {
+            const float m0 = row_bit(kb, 2 * k) ? p.drop_rscale : 0.f;
+            const float m1 = row_bit(kb, 2 * k + 1) ? p.drop_rscale : 0.f;
+            gd = f2_fma(g2, f2(m0, m1), nd2);
+          } else {
+            gd = f2_add(g2, nd2);
+          }
           float a0, a1;
           f2_split(f2_mul(f2(__uint_as_float(sr[k >> 4][(2 * k) & 31]),
-                             __uint_as_float(sr[k >> 4][(2 * k + 1) & 31])),
-                          f2_add(f2(__uint_as_float(dr[k >> 4][(2 * k) & 31]),
-                                    __uint_as_float(dr[k >> 4][(2 * k + 1) & 31])), nd2)),
+                             __uint_as_float(sr[k >> 4][(2 * k + 1) & 31])), gd),
                    a0, a1);
           pk[k] = pack2<BF16>(a0, a1);
         }
@@ -491,7 +510,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 // CTA item: (bh, key tile kt). Streams Q_i, dO_i; per query tile:
 //   S^T = K Q_i^T, dP^T = V dO_i^T  (TMEM)  ->  P^T, dS^T (16-bit, over them)
 //   ->  dV += P^T dO_i,  dK += dS^T Q_i
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -711,6 +730,25 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       const int key = k0 + r;
       for (int i = 0; i < n_q; ++i) {
         const int q0 = (i0 + i) * BM;
+        // dropout: bit (c & 31) of zb[c >> 5] is the keep bit of query
+        // q0 + 64 hf + c (c < 64) for this thread's key. Each lane of a 16-key group draws the
+        // call of one query row for its group; a shuffle hands the group's 16-bit mask on.
+        uint32_t zb[2] = {0, 0};
+        if constexpr (DROP) {
+          const uint32_t grp = (uint32_t)((k0 + wq * 32) >> 4) + (uint32_t)(lane >> 4);
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint32_t qrow = (uint32_t)(q0 + hf * 64 + blk * 16 + (lane & 15));
+            const uint32_t m16 = keep16(dropout_words(grp, qrow, (uint32_t)bh, p.drop_offset,
+                                                      p.drop_keys), p.drop_bias);
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) {
+              const uint32_t v = __shfl_sync(0xffffffffu, m16, (lane & 16) | ii);
+              const int c = blk * 16 + ii;
+              zb[c >> 5] |= ((v >> (lane & 15)) & 1u) << (c & 31);
+            }
+          }
+        }
         // this query tile's L log2(e) (staged by half 0) and D (by half 1), one value per
         // thread (rows past Nq: L = +inf so that P = 0); the previous tile's readers
         // finished at the barrier that ended its iteration
@@ -774,12 +812,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           for (int kk = 0; kk < 16; ++kk) {
             const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + hf * 64 + c * 32 + 2 * kk);
             const float p0 = __uint_as_float(sr[c][2 * kk]), p1 = __uint_as_float(sr[c][2 * kk + 1]);
+            const uint64_t g2 = f2(__uint_as_float(dr[c][2 * kk]), __uint_as_float(dr[c][2 * kk + 1]));
             float a0, a1;
-            f2_split(f2_mul(f2(p0, p1),
-                            f2_add(f2(__uint_as_float(dr[c][2 * kk]), __uint_as_float(dr[c][2 * kk + 1])),
-                                   f2(-dd.x, -dd.y))),
-                     a0, a1);
-            pp[kk] = pack2<BF16>(p0, p1);
+            if constexpr (DROP) {
+              // dV takes P o Z (the 1/(1-p) of Z is applied to dV at the end), dP^T takes Z
+              const uint32_t z0 = (zb[c] >> (2 * kk)) & 1u, z1 = (zb[c] >> (2 * kk + 1)) & 1u;
+              f2_split(f2_mul(f2(p0, p1), f2_fma(g2, f2(z0 ? p.drop_rscale : 0.f, z1 ? p.drop_rscale : 0.f),
+                                                 f2(-dd.x, -dd.y))),
+                       a0, a1);
+              pp[kk] = pack2<BF16>(z0 ? p0 : 0.f, z1 ? p1 : 0.f);
+            } else {
+              f2_split(f2_mul(f2(p0, p1), f2_add(g2, f2(-dd.x, -dd.y))), a0, a1);
+              pp[kk] = pack2<BF16>(p0, p1);
+            }
             pd[kk] = pack2<BF16>(a0, a1);
           }
           tmem_st16(tPT + c * 16, pp);
@@ -814,8 +859,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         tmem_ld32(tV + q * 32, o);
         tmem_wait_ld();
         reg_fence(o);
+        const float vs = DROP ? p.drop_rscale : 1.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1]));
+        for (int k = 0; k < 16; ++k)
+          w16[k] = pack2<BF16>(__uint_as_float(o[2 * k]) * vs, __uint_as_float(o[2 * k + 1]) * vs);
         if (valid) store_row16(p.dV, grow, D, q, w16);
       }
       tc_fence_before();

@@ -1194,13 +1194,13 @@ int run_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int 
 }
 
 // ---------------------------------------------------------------------------- backward
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const CUtensorMap& mdo, BwdParams p, DeviceInfo* di, cudaStream_t st) {
   using LY = BwdLayout<D>;
   using LQ = DqLayout<D>;
-  auto kq = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
-  auto kkv = fa_bwd_dkv_kernel<D, BF16, CAUSAL>;
+  auto kq = fa_bwd_dq_kernel<D, BF16, CAUSAL, DROP>;
+  auto kkv = fa_bwd_dkv_kernel<D, BF16, CAUSAL, DROP>;
   static bool attr_set[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
@@ -1224,6 +1224,23 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   kkv<<<grid, BW_THREADS, LY::SMEM_BYTES, st>>>(mk, mv, mq, mdo, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <bool DROP>
+int dispatch_bwd(int d, bool bf16, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+                 const CUtensorMap& mv, const CUtensorMap& mdo, const BwdParams& p, DeviceInfo* di,
+                 cudaStream_t st) {
+  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch_bwd<64, false, false, DROP>(mq, mk, mv, mdo, p, di, st);
+    case 1: return launch_bwd<64, false, true, DROP>(mq, mk, mv, mdo, p, di, st);
+    case 2: return launch_bwd<64, true, false, DROP>(mq, mk, mv, mdo, p, di, st);
+    case 3: return launch_bwd<64, true, true, DROP>(mq, mk, mv, mdo, p, di, st);
+    case 4: return launch_bwd<128, false, false, DROP>(mq, mk, mv, mdo, p, di, st);
+    case 5: return launch_bwd<128, false, true, DROP>(mq, mk, mv, mdo, p, di, st);
+    case 6: return launch_bwd<128, true, false, DROP>(mq, mk, mv, mdo, p, di, st);
+    default: return launch_bwd<128, true, true, DROP>(mq, mk, mv, mdo, p, di, st);
+  }
 }
 
 size_t bwd_ws_bytes(long long BH, int Nq) {
@@ -1350,10 +1367,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   return bwd_ws_bytes((long long)B * H, Nq);
 }
 
-int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-           const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
-           float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
-           void* stream) {
+static int run_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                   size_t workspace_bytes, void* stream, const DropArgs* drop) {
   bool noop = false;
   // Q, K, V as in the forward; O stands in for the output argument of the shared checks
   int rc = check_args(Q, K, V, const_cast<void*>(O), const_cast<float*>(L), B, H, Nq, Nk, d, scale,
@@ -1390,19 +1407,43 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
   p.c = scale * 1.4426950408889634f;
   p.scale = scale;
   p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.drop_bias = 0;
+  p.drop_offset = 0;
+  p.drop_rscale = 1.f;
+  p.drop_keys = philox_keys(0);
+  if (drop) {
+    p.drop_bias = dropout_bias(drop->t);
+    p.drop_keys = philox_keys(drop->seed);
+    p.drop_offset = drop->offset;
+    p.drop_rscale = (float)(256.0 / (256.0 - (double)drop->t));
+  }
   if ((long long)p.n_qt * BH > 0x7fffffffLL || (long long)p.n_kt * BH > 0x7fffffffLL) return FA_ERR_SHAPE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
-  switch (key) {
-    case 0: return launch_bwd<64, false, false>(mq, mk, mv, mdo, p, di, st);
-    case 1: return launch_bwd<64, false, true>(mq, mk, mv, mdo, p, di, st);
-    case 2: return launch_bwd<64, true, false>(mq, mk, mv, mdo, p, di, st);
-    case 3: return launch_bwd<64, true, true>(mq, mk, mv, mdo, p, di, st);
-    case 4: return launch_bwd<128, false, false>(mq, mk, mv, mdo, p, di, st);
-    case 5: return launch_bwd<128, false, true>(mq, mk, mv, mdo, p, di, st);
-    case 6: return launch_bwd<128, true, false>(mq, mk, mv, mdo, p, di, st);
-    default: return launch_bwd<128, true, true>(mq, mk, mv, mdo, p, di, st);
-  }
+  return drop ? dispatch_bwd<true>(d, bf16, causal, mq, mk, mv, mdo, p, di, st)
+              : dispatch_bwd<false>(d, bf16, causal, mq, mk, mv, mdo, p, di, st);
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+           const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
+           float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+           void* stream) {
+  return run_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+                 workspace_bytes, stream, nullptr);
+}
+
+int fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, fa_dtype dtype, float p_drop,
+                   unsigned long long seed, unsigned int offset, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  uint32_t t = 0;
+  if (!dropout_threshold(p_drop, &t)) return FA_ERR_DROPOUT;
+  if (t == 0)  // nothing was dropped: the plain backward pass
+    return run_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+                   workspace_bytes, stream, nullptr);
+  const DropArgs da{t, seed, offset};
+  return run_bwd(Q, K, V, O, dO, L, dQ, dK, dV, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+                 workspace_bytes, stream, &da);
 }
 
 int fa_last_status(void) {

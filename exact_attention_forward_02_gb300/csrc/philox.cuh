@@ -84,14 +84,15 @@ __device__ __forceinline__ uint4 dropout_words(uint32_t g, uint32_t i, uint32_t 
   return philox4x32_10(make_uint4(g, i, bh, offset), k);
 }
 
-// The keep bits of one query row over 128 consecutive keys starting at 16 g0, packed for
+// The keep bits of one query row over 32 NW consecutive keys starting at 16 g0, packed for
 // the masking of 16-bit probability pairs: word q holds key pairs (32q + 2kk, 32q + 2kk + 1)
 // for kk = 0..15 as bit kk (even key) and bit 16 + kk (odd key).
+template <int NW = 4>
 __device__ __forceinline__ void dropout_row_bits(uint32_t g0, uint32_t i, uint32_t bh,
                                                  uint32_t offset, const PhiloxKeys& k,
-                                                 uint32_t bias, uint32_t bits[4]) {
+                                                 uint32_t bias, uint32_t* bits) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < NW; ++q) {
     uint4 r2[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) r2[h] = dropout_words(g0 + 2 * q + h, i, bh, offset, k);
@@ -113,6 +114,25 @@ __device__ __forceinline__ void dropout_row_bits(uint32_t g0, uint32_t i, uint32
 // The 16-bit lane mask of key pair kk of a word of dropout_row_bits.
 __device__ __forceinline__ uint32_t pair_mask(uint32_t bits_word, int kk) {
   return spread_flags2(bits_word << (15 - kk));
+}
+
+// Whether key e (0..63) of a dropout_row_bits row is kept, as 0 or 1.
+__device__ __forceinline__ uint32_t row_bit(const uint32_t* bits, int e) {
+  const int pr = e >> 1, kk = pr & 15;
+  return (bits[pr >> 4] >> ((e & 1) ? 16 + kk : kk)) & 1u;
+}
+
+// The keep mask of the sixteen keys of one generator call: bit e for key 16 g + e.
+__device__ __forceinline__ uint32_t keep16(const uint4& w, uint32_t bias) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t f0, f1;
+    keep_flags4(uint4_word(w, q), bias, f0, f1);
+    m |= ((f0 >> 8) & 1u) << (4 * q) | ((f0 >> 24) & 1u) << (4 * q + 1) |
+         ((f1 >> 8) & 1u) << (4 * q + 2) | ((f1 >> 24) & 1u) << (4 * q + 3);
+  }
+  return m;
 }
 
 }  // namespace fa

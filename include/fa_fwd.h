@@ -206,6 +206,21 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const voi
            float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
            void* stream);
 
+/* fa_bwd_dropout -- the backward pass of fa_fwd_dropout ("Flash Attention" page,
+ * "Algorithm 4": the mask Z is regenerated from the forward's generator state, here
+ * (p_drop, seed, offset), which must be the forward call's):
+ *     dV = (P o Z)^T dO,  dP = (dO V^T) o Z,  D_i = rowsum(dO_i o O_i),  dS = P o (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q
+ * with Z_ij = 256 / (256 - t) where fa_fwd_dropout kept (i, j) and 0 where it dropped it
+ * (the mask of fa_fwd_dropout). O is the dropout forward's output, L its logsumexp.
+ * Arguments, layout, workspace and errors as fa_bwd, plus FA_ERR_DROPOUT for a bad p_drop;
+ * p_drop with t = 0 runs fa_bwd. */
+int fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* L, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, fa_dtype dtype, float p_drop,
+                   unsigned long long seed, unsigned int offset, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
 /* fa_last_status -- synchronise the current device, then return the device-side status
  * word of libfa on that device: FA_OK, or the first error a kernel recorded since the
  * last fa_clear_status() (FA_ERR_TIMEOUT when a bounded pipeline wait gave up; the kernel
