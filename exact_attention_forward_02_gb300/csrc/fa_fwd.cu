@@ -250,6 +250,23 @@ __device__ __forceinline__ bool sched_next(Sched& s, Item& it, const Params& p) 
   return true;
 }
 
+// Maximum of the N values of t as a balanced tree of three-input maxima; t is consumed.
+template <int N>
+__device__ __forceinline__ float tree_max(float* t) {
+  if constexpr (N == 1) {
+    return t[0];
+  } else {
+    constexpr int M = (N + 2) / 3;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const float y = 3 * i + 1 < N ? t[3 * i + 1] : -INFINITY;
+      const float z = 3 * i + 2 < N ? t[3 * i + 2] : -INFINITY;
+      t[i] = max3(t[3 * i], y, z);
+    }
+    return tree_max<M>(t);
+  }
+}
+
 // ----------------------------------------------------------------------------- kernel
 // BF16: type of O (and of Q, K, V unless FP8). FP8: Q, K are E4M3 [BH, N, D] and tmV maps
 // V^T, E4M3 [BH, D, ldvt] (keys contiguous), so that V is a K-major operand of P V.
@@ -551,18 +568,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int vis = kv_lim - (it.j0 + j) * BN;
         const bool full = vis >= BN;
         auto sv = [&](int k) { return __uint_as_float(sr[k >> 5][k & 31]); };
-        // raw row max over the visible keys (three-input max, four chains)
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (full) {
+        // raw row max over the visible keys: a balanced tree of three-input maxima (depth 5
+        // for 128 keys, against 16 for four running chains)
+        float mt;
+        {
+          float t[43];
+          if (full) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) mx[k & 3] = max3(mx[k & 3], sv(2 * k), sv(2 * k + 1));
-        } else {
+            for (int i = 0; i < 42; ++i) t[i] = max3(sv(3 * i), sv(3 * i + 1), sv(3 * i + 2));
+            t[42] = fmaxf(sv(126), sv(127));
+          } else {
+            auto mv = [&](int e) { return e < vis ? sv(e) : -INFINITY; };
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            mx[k & 3] = max3(mx[k & 3], 2 * k < vis ? sv(2 * k) : -INFINITY,
-                             2 * k + 1 < vis ? sv(2 * k + 1) : -INFINITY);
+            for (int i = 0; i < 42; ++i) t[i] = max3(mv(3 * i), mv(3 * i + 1), mv(3 * i + 2));
+            t[42] = fmaxf(mv(126), mv(127));
+          }
+          mt = tree_max<43>(t);
         }
-        const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
         const float m_tile = (mt == -INFINITY) ? -INFINITY : mt * c;
         float m_new = m_run, alpha = 1.f;
         bool rescale = false;
