@@ -53,6 +53,11 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    lib.fa_fwd_host.restype = ctypes.c_int
+    lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
+        ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_fwd_host_workspace_bytes.argtypes = [ctypes.c_int] * 5
     lib.fa_fwd_dropout.restype = ctypes.c_int
     lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
         ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
@@ -114,6 +119,18 @@ def fa_fwd_noalloc(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, stream)
     """C-ABI call of the allocation-free variant (fixed device scratch, see fa_fwd.h)."""
     return int(lib.fa_fwd_noalloc(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
                                   float(scale), int(bool(causal)), int(dtype), stream))
+
+
+def fa_fwd_host(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+                workspace_bytes, stream) -> int:
+    """C-ABI call of the forward pass on HOST buffers (device workspace; see fa_fwd.h)."""
+    return int(lib.fa_fwd_host(Q, K, V, O, L, int(B), int(H), int(Nq), int(Nk), int(d),
+                               float(scale), int(bool(causal)), int(dtype), workspace,
+                               int(workspace_bytes), stream))
+
+
+def fa_fwd_host_workspace_bytes(B, H, Nq, Nk, d) -> int:
+    return int(lib.fa_fwd_host_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(d)))
 
 
 def fa_fwd_dropout(Q, K, V, O, L, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset,

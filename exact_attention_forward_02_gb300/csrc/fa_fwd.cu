@@ -1287,9 +1287,142 @@ int noalloc_scratch(void** out) {
   return FA_OK;
 }
 
+// ------------------------------------------------------------------------ host buffers
+// fa_fwd_host: chunks of heads stream through a ring of device slots in the caller's
+// workspace. One library stream carries every host-to-device copy and one every
+// device-to-host copy (one queue per copy direction, so that both directions run at
+// once), and one stream per slot runs the slot's attention launches; per-slot events
+// chain them: inputs in -> launch -> outputs out -> slot free for the next chunk.
+constexpr int HOST_SLOTS = 4;
+constexpr int HOST_CHUNKS = 8;  // chunks per call when there are enough heads
+
+struct HostPipe {
+  bool ok = false;
+  cudaStream_t h2d, d2h, comp[HOST_SLOTS];
+  cudaEvent_t start, in[HOST_SLOTS], out[HOST_SLOTS], freed[HOST_SLOTS], h2d_done, d2h_done,
+      comp_done[HOST_SLOTS];
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;  // held while a call enqueues its work (the streams and events are shared)
+
+int host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ok) {
+    auto mk_stream = [](cudaStream_t* st) { return cudaStreamCreateWithFlags(st, cudaStreamNonBlocking) == cudaSuccess; };
+    auto mk_event = [](cudaEvent_t* ev) { return cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess; };
+    bool good = mk_stream(&hp.h2d) && mk_stream(&hp.d2h) && mk_event(&hp.start) &&
+                mk_event(&hp.h2d_done) && mk_event(&hp.d2h_done);
+    for (int s = 0; good && s < HOST_SLOTS; ++s)
+      good = mk_stream(&hp.comp[s]) && mk_event(&hp.in[s]) && mk_event(&hp.out[s]) &&
+             mk_event(&hp.freed[s]) && mk_event(&hp.comp_done[s]);
+    if (!good) return FA_ERR_CUDA;
+    hp.ok = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+struct HostChunks {
+  long long hc, n;             // heads per chunk, number of chunks
+  size_t q, kv, o, l;          // bytes per head of Q (and O), of K (and V), of O, of L
+  size_t off_k, off_v, off_o, off_l, slot;  // layout of one slot
+  int slots;
+};
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+HostChunks host_chunks(long long BH, int Nq, int Nk, int d) {
+  HostChunks c;
+  c.hc = (BH + HOST_CHUNKS - 1) / HOST_CHUNKS;
+  c.n = (BH + c.hc - 1) / c.hc;
+  c.q = (size_t)Nq * d * 2;
+  c.kv = (size_t)Nk * d * 2;
+  c.o = c.q;
+  c.l = (size_t)Nq * 4;
+  c.off_k = align256(c.hc * c.q);
+  c.off_v = c.off_k + align256(c.hc * c.kv);
+  c.off_o = c.off_v + align256(c.hc * c.kv);
+  c.off_l = c.off_o + align256(c.hc * c.o);
+  c.slot = c.off_l + align256(c.hc * c.l);
+  c.slots = (int)(c.n < HOST_SLOTS ? c.n : HOST_SLOTS);
+  return c;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+  const HostChunks c = host_chunks((long long)B * H, Nq, Nk, d);
+  return (size_t)c.slots * c.slot;
+}
+
+int fa_fwd_host(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H,
+                int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  bool noop = false;
+  int rc = check_args(Q, K, V, O, L, B, H, Nq, Nk, d, scale, dtype, &noop);
+  if (rc != FA_OK || noop) return rc;
+  const long long BH = (long long)B * H;
+  const HostChunks c = host_chunks(BH, Nq, Nk, d);
+  if (!workspace || workspace_bytes < (size_t)c.slots * c.slot) return FA_ERR_WORKSPACE;
+  if ((uintptr_t)workspace & 255) return FA_ERR_ALIGN;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != FA_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  if ((rc = host_pipe(dev, &hp)) != FA_OK) return rc;
+  cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // everything starts after the work already queued on the caller's stream
+  if (!ok(cudaEventRecord(hp->start, caller)) || !ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+      !ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
+    return FA_ERR_CUDA;
+  for (int s = 0; s < c.slots; ++s)
+    if (!ok(cudaStreamWaitEvent(hp->comp[s], hp->start, 0))) return FA_ERR_CUDA;
+  const uint8_t* hq = static_cast<const uint8_t*>(Q);
+  const uint8_t* hk = static_cast<const uint8_t*>(K);
+  const uint8_t* hv = static_cast<const uint8_t*>(V);
+  uint8_t* ho = static_cast<uint8_t*>(O);
+  uint8_t* hl = reinterpret_cast<uint8_t*>(L);
+  for (long long ch = 0; ch < c.n; ++ch) {
+    const int s = (int)(ch % c.slots);
+    uint8_t* base = static_cast<uint8_t*>(workspace) + (size_t)s * c.slot;
+    const long long h0 = ch * c.hc;
+    const long long nh = (BH - h0) < c.hc ? (BH - h0) : c.hc;
+    // inputs: once the slot's previous chunk has left it
+    if (ch >= c.slots && !ok(cudaStreamWaitEvent(hp->h2d, hp->freed[s], 0))) return FA_ERR_CUDA;
+    if (!ok(cudaMemcpyAsync(base, hq + h0 * c.q, nh * c.q, cudaMemcpyHostToDevice, hp->h2d)) ||
+        !ok(cudaMemcpyAsync(base + c.off_k, hk + h0 * c.kv, nh * c.kv, cudaMemcpyHostToDevice, hp->h2d)) ||
+        !ok(cudaMemcpyAsync(base + c.off_v, hv + h0 * c.kv, nh * c.kv, cudaMemcpyHostToDevice, hp->h2d)) ||
+        !ok(cudaEventRecord(hp->in[s], hp->h2d)))
+      return FA_ERR_CUDA;
+    // the attention launch on the slot's stream
+    if (!ok(cudaStreamWaitEvent(hp->comp[s], hp->in[s], 0))) return FA_ERR_CUDA;
+    rc = run(base, base + c.off_k, base + c.off_v, base + c.off_o,
+             reinterpret_cast<float*>(base + c.off_l), 1, (int)nh, Nq, Nk, d, scale, causal, dtype,
+             nullptr, 0, false, hp->comp[s]);
+    if (rc != FA_OK) return rc;
+    if (!ok(cudaEventRecord(hp->out[s], hp->comp[s]))) return FA_ERR_CUDA;
+    // outputs
+    if (!ok(cudaStreamWaitEvent(hp->d2h, hp->out[s], 0)) ||
+        !ok(cudaMemcpyAsync(ho + h0 * c.o, base + c.off_o, nh * c.o, cudaMemcpyDeviceToHost, hp->d2h)) ||
+        !ok(cudaMemcpyAsync(hl + h0 * c.l, base + c.off_l, nh * c.l, cudaMemcpyDeviceToHost, hp->d2h)) ||
+        !ok(cudaEventRecord(hp->freed[s], hp->d2h)))
+      return FA_ERR_CUDA;
+  }
+  // the caller's stream waits for all of it (the device-to-host stream finishes last, and
+  // waiting for the others as well leaves no library work behind the caller's back)
+  if (!ok(cudaEventRecord(hp->h2d_done, hp->h2d)) || !ok(cudaEventRecord(hp->d2h_done, hp->d2h)) ||
+      !ok(cudaStreamWaitEvent(caller, hp->h2d_done, 0)) || !ok(cudaStreamWaitEvent(caller, hp->d2h_done, 0)))
+    return FA_ERR_CUDA;
+  for (int s = 0; s < c.slots; ++s)
+    if (!ok(cudaEventRecord(hp->comp_done[s], hp->comp[s])) ||
+        !ok(cudaStreamWaitEvent(caller, hp->comp_done[s], 0)))
+      return FA_ERR_CUDA;
+  return FA_OK;
+}
 
 int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, fa_dtype dtype, void* stream) {

@@ -127,6 +127,31 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    fa_dtype dtype, void* stream);
 
+/* fa_fwd_host -- fa_fwd on HOST buffers: Q, K, V are read from and O, L written to host
+ * memory, with the copies overlapped with the computation.
+ * The heads are processed in up to 8 chunks that stream through a ring of up to 4 device
+ * slots in `workspace`. Library streams carry the work: one takes every host-to-device
+ * copy, one every device-to-host copy (so both directions run at once), and each slot
+ * has one for its attention launches. Events chain them per slot: inputs in, launch,
+ * outputs out, slot free for the next chunk.
+ * Same results, arguments and errors as fa_fwd, except:
+ *   Q, K, V, O, L  HOST pointers, same layout and alignment as fa_fwd. Make them
+ *                  page-locked (cudaHostAlloc / cudaHostRegister), or the copies cannot
+ *                  overlap the computation (the results are the same either way).
+ *   workspace      DEVICE pointer, 256-byte aligned, at least fa_fwd_host_workspace_bytes()
+ *                  bytes (no initialisation needed).
+ *   stream         the library's streams start after the work queued on `stream` so far,
+ *                  and `stream` waits for them: O and L are in host memory once `stream`
+ *                  has been synchronised.
+ * Calls from several host threads on one device are serialised while they queue their
+ * work (the library's streams are shared); calls that overlap on the GPU need their own
+ * workspaces and host buffers that do not alias. FA_ERR_WORKSPACE for a missing or small
+ * workspace. */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+int fa_fwd_host(const void* Q, const void* K, const void* V, void* O, float* L,
+                int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
 /* fa_fwd_dropout -- the forward pass with dropout on the attention probabilities
  * ("Flash Attention" page, "Algorithm 2": P_dropped = dropout(P, p_drop), O = P_dropped V;
  * the forward returns the generator state, here the pair (seed, offset)):

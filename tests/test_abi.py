@@ -122,3 +122,19 @@ def test_dropout_host_checks():
     assert fa.fa_dropout_mask(0, 1, 1, 0, 8, 0.1, 1, 2, None) == fa.FA_OK
     assert fa.fa_dropout_mask(0, 1, 1, 8, 8, 0.1, 1, 2, None) == fa.FA_ERR_NULL
     assert fa.fa_dropout_mask(P, -1, 1, 8, 8, 0.1, 1, 2, None) == fa.FA_ERR_SHAPE
+
+
+def test_host_buffer_api_host_checks():
+    import exact_attention_forward_02_gb300 as fa
+    base = (P, P, P, P, P, 1, 1, 128, 128, 64, 0.125, 0, 1)
+    need = fa.fa_fwd_host_workspace_bytes(1, 1, 128, 128, 64)
+    assert need >= 128 * 64 * 2 * 4 + 128 * 4
+    assert fa.fa_fwd_host_workspace_bytes(1, 1, 128, 128, 96) == 0
+    assert fa.fa_fwd_host(*base, 0, 0, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_fwd_host(*base, P, need - 1, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_fwd_host(*base, P + 16, need, None) == fa.FA_ERR_ALIGN
+    assert fa.fa_fwd_host(0, *base[1:], P, need, None) == fa.FA_ERR_NULL
+    assert fa.fa_fwd_host(*base[:9], 96, *base[10:], P, need, None) == fa.FA_ERR_HEAD_DIM
+    # more heads than chunks: several heads per chunk, at most four slots
+    assert fa.fa_fwd_host_workspace_bytes(2, 8, 4096, 4096, 128) == 4 * (
+        2 * (4096 * 128 * 2) * 4 + ((2 * 4096 * 4 + 255) // 256) * 256)
