@@ -112,7 +112,8 @@ struct Params {
   // stream-K split of the key range (full attention with a workspace): the flattened
   // (item, K/V tile) sequence is cut into gridDim.x equal contiguous ranges
   int streamk;
-  float* ws_part;  // partial rows: [CTA][slot 2][Q tile 2][128 rows][D + 4] fp32 (O~, m, l, pad)
+  float* ws_part;  // partial states: [CTA][slot 2][Q tile 2][D + 2][128 rows] fp32 (O~, m, l),
+                   // stored column by column so that a warp's accesses are coalesced
   int* ws_cnt;     // per (item, Q tile, row): K/V tiles accounted for; back to 0 after use
 };
 
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   static_assert(!(FP8 && DROP), "dropout is not combined with E4M3 inputs");
   static_assert(!FP8 || D == 128, "E4M3 inputs need d = 128 (one 128-byte row per tile row)");
   using LY = Layout<D, FP8 ? 1 : 2>;
-  constexpr int PART_ROW = D + 4;  // O~[D], m, l, 2 pad: rows stay 16-byte aligned
+  constexpr int PART_COLS = D + 2;  // O~[D], m, l of a row, each column stored for 128 rows
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -732,20 +733,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // ("Flash Attention" page, section "平行化": partial states merge with the
           // associative operator), then the CTA that brings the item's count of merged
           // K/V tiles to the total merges every piece of the item.
-          float* prow = p.ws_part + ((((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * BM + r) * PART_ROW;
+          float* pcol = p.ws_part + (((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * PART_COLS * BM + r;
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             tmem_ld32(tO + q * 32, o);
             tmem_wait_ld();
             reg_fence(o);
-            float4* dst = reinterpret_cast<float4*>(prow + q * 32);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              __stcg(dst + v, make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                          __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+            for (int k = 0; k < 32; ++k) __stcg(pcol + (q * 32 + k) * BM, __uint_as_float(o[k]));
           }
-          __stcg(reinterpret_cast<float2*>(prow + D), make_float2(m_run, l_run));
+          __stcg(pcol + D * BM, m_run);
+          __stcg(pcol + (D + 1) * BM, l_run);
           tc_fence_before();
           // one counter per query row: this thread's row merges independently of the
           // other rows, so no synchronisation inside the warpgroup is needed
@@ -759,16 +758,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const long long G = gridDim.x;
             const long long ub = (long long)it.item * p.n_kv_all;
             const int c0 = sk_owner(ub, W, G), c1 = sk_owner(ub + p.n_kv_all - 1, W, G);
-            auto piece_row = [&](int cc) -> const float* {
-              const int slot = sk_bound(cc, W, G) >= ub ? 0 : 1;
-              return p.ws_part + ((((size_t)cc * 2 + slot) * 2 + g) * BM + r) * PART_ROW;
+            // the first piece is its CTA's last one (slot 1) unless that CTA's range starts
+            // with this item; every later piece is its CTA's first (slot 0)
+            const int slot0 = sk_bound(c0, W, G) < ub ? 1 : 0;
+            auto piece = [&](int cc) -> const float* {
+              return p.ws_part +
+                     (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
             };
             float m = -INFINITY;
-            for (int cc = c0; cc <= c1; ++cc) m = fmaxf(m, __ldcg(piece_row(cc) + D));
+            for (int cc = c0; cc <= c1; ++cc) m = fmaxf(m, __ldcg(piece(cc) + D * BM));
             float l = 0.f;
             for (int cc = c0; cc <= c1; ++cc) {
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(piece_row(cc) + D));
-              l += ml.y * ex2_approx(ml.x - m);
+              const float* pc = piece(cc);
+              l += __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
             }
             float inv_l = l > 0.f ? 1.f / l : 0.f;
             if constexpr (DROP) inv_l *= p.drop_rscale;
@@ -781,17 +783,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int k = 0; k < 32; ++k) acc[k] = 0.f;
               for (int cc = c0; cc <= c1; ++cc) {
-                const float* pr = piece_row(cc);
-                const float wgt = ex2_approx(__ldcg(pr + D) - m) * inv_l;
-                const float4* src = reinterpret_cast<const float4*>(pr + q * 32);
+                const float* pc = piece(cc);
+                // the chunk's 32 loads are independent: issue them all before the products
+                float x[32];
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  const float4 x = __ldcg(src + v);
-                  acc[4 * v] = fmaf(x.x, wgt, acc[4 * v]);
-                  acc[4 * v + 1] = fmaf(x.y, wgt, acc[4 * v + 1]);
-                  acc[4 * v + 2] = fmaf(x.z, wgt, acc[4 * v + 2]);
-                  acc[4 * v + 3] = fmaf(x.w, wgt, acc[4 * v + 3]);
-                }
+                for (int k = 0; k < 32; ++k) x[k] = __ldcg(pc + (q * 32 + k) * BM);
+                const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = fmaf(x[k], wgt, acc[k]);
               }
               if (valid) {
                 uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
