@@ -37,7 +37,7 @@ FP8_DOMINANT = "b2h8_n8192_d128_causal_fp8"
 FP8_OVER_BF16 = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FLUSH_BYTES = 256 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
-KERNEL_SOURCES = ("exact_attention_forward_02_gb300/csrc/fa_fwd.cu",
+KERNEL_SOURCES = ("exact_attention_forward_02_gb300/csrc/fa_fwd_kernel.cuh",
                   "exact_attention_forward_02_gb300/csrc/sm103_ptx.cuh",
                   "exact_attention_forward_02_gb300/csrc/philox.cuh")
 

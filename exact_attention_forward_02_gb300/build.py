@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc", "fa_fwd.cu")
 DEPS = [SRC, os.path.join(PKG, "csrc", "sm103_ptx.cuh"), os.path.join(PKG, "csrc", "fa_bwd.cuh"),
-        os.path.join(PKG, "csrc", "philox.cuh"),
+        os.path.join(PKG, "csrc", "philox.cuh"), os.path.join(PKG, "csrc", "fa_fwd_kernel.cuh"),
         os.path.join(ROOT, "include", "fa_fwd.h")]
 LIB = os.path.join(PKG, "libfa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,823 @@
+// fa_fwd_kernel.cuh -- the forward attention kernel (device code). Included by fa_fwd.cu.
+//
+// What it computes (CS336 lecture 5 "05_flash_attention.py", part 2, flash_attention_forward;
+// "Flash Attention" (blog.cyberangel.work), sections "Online Softmax" and "平行化"):
+// for each query tile Q_i and each key/value tile (K_j, V_j), in order of j,
+//     S    = tau * Q_i K_j^T            (masked to -inf where a key is not visible)
+//     m'   = max(m, rowmax(S))
+//     P    = exp(S - m')
+//     l    = exp(m - m') l + rowsum(P)
+//     O~   = exp(m - m') O~ + P V_j
+// and finally O = O~ / l, L = m + ln l. The scores never leave the SM.
+//
+// With dropout ("Flash Attention" page, "Algorithm 2") the P fed to the second product is
+// masked by the Philox mask of philox.cuh, l stays the sum of the undropped P, and the
+// epilogue divides by l (1 - p).
+//
+// GB300 mapping (one persistent CTA per SM, 12 warps):
+//   warp 8      TMA producer: loads the two 128-row Q tiles of a work item once, then
+//               streams K_j, V_j through a ring of shared-memory slots (mbarrier pipeline).
+//   warp 9      MMA issuer for both Q tiles (warp-converged, one elected lane): issues
+//               tcgen05.mma for S = Q K^T (both operands K-major in shared memory, fp32
+//               accumulator in Tensor Memory) and O~ += P V (P read from Tensor Memory,
+//               V MN-major in shared memory), and signals completion with tcgen05.commit.
+//   warps 10,11 no role (they keep the register split of whole warpgroups).
+//   warps 0-7   two softmax warpgroups, one per Q tile (ping-pong): thread r owns query
+//               row r of its tile (TMEM lane r), reads its 128 scores with tcgen05.ld,
+//               applies the mask, keeps (m, l) in registers in base-2 units (the scale is
+//               folded with log2(e)), writes P as 16-bit values over its scores in Tensor
+//               Memory, rescales O~ in TMEM when the running max grows by more than 2^8,
+//               and runs the epilogue.
+// Work items are (batch*head, 256-row query block); causal items run heaviest first.
+#pragma once
+
+#include <cuda.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_fwd.h"
+#include "philox.cuh"
+#include "sm103_ptx.cuh"
+
+// Device-side status word (one per device that loads the library; this header is compiled
+// once, as part of fa_fwd.cu).
+__device__ int g_fa_status;
+
+namespace fa {
+
+constexpr int BM = 128;                  // query rows per tile = TMEM lanes
+constexpr int BN = 128;                  // keys per K/V tile
+constexpr int NUM_WARPS = 12;            // three warpgroups: softmax 0, softmax 1, load/MMA
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int WARP_LOAD = 8;
+constexpr int WARP_MMA = 9;              // issues every MMA and owns the TMEM allocation
+// Register split (launch: 384 threads x 168): the load/MMA warpgroup gives registers
+// to the two softmax warpgroups: 2*128*200 + 128*104 = 64512 = 384*168.
+constexpr uint32_t REGS_SOFTMAX = 200;
+constexpr uint32_t REGS_OTHER = 104;
+constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O0 | O1, 128 columns each
+constexpr uint32_t TMEM_S0 = 0, TMEM_O0 = 256;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O~ only when m grows > 2^8
+constexpr int SMEM_LIMIT = 232448;       // 227 KB opt-in dynamic shared memory per CTA
+constexpr int MAX_SLOTS = 8;
+
+struct Barriers {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[MAX_SLOTS];
+  uint64_t kv_release[MAX_SLOTS];  // release unit m = {V of tile m-1, K of tile m}
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// ESZ: bytes per input element (2 for fp16/bf16, 1 for E4M3)
+template <int D, int ESZ = 2>
+struct Layout {
+  static constexpr int TILE_BYTES = BM * D * ESZ;     // one Q, K or V tile (V^T for E4M3)
+  static constexpr int CHUNK_BYTES = BM * 128;        // 128 rows x one 128-byte swizzle span
+  static constexpr int CHUNKS = D * ESZ / 128;        // 128-byte spans per row
+  static constexpr int CHUNK_ELEMS = 128 / ESZ;       // elements per span
+  static constexpr int FIXED = 2 * TILE_BYTES + 1024 /*align*/ + 512 /*bars*/;
+  static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TILE_BYTES;
+  static constexpr int KV_SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + KV_SLOTS * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(Barriers) + 1024;
+  static_assert(KV_SLOTS >= 2, "need at least two K/V slots");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+};
+
+struct Params {
+  void* O;
+  float* L;
+  int BH, Nq, Nk;
+  int n_qblk;      // ceil(Nq / 256)
+  int n_items;     // n_qblk * BH
+  int n_kv_all;    // ceil(Nk / 128)
+  float c;         // scale * log2(e)
+  unsigned long long wait_limit_ns;
+  // dropout (kernels instantiated with DROP only)
+  uint32_t drop_bias;    // (0x100 - t) * 0x00010001 for the 8-bit threshold t
+  uint32_t drop_offset;  // counter word 3
+  float drop_rscale;     // 256 / (256 - t)
+  PhiloxKeys drop_keys;  // round keys of the seed
+  float o_scale;         // extra factor on O (the V descale of E4M3 inputs; 1 otherwise)
+  // stream-K split of the key range (full attention with a workspace): the flattened
+  // (item, K/V tile) sequence is cut into gridDim.x equal contiguous ranges
+  int streamk;
+  float* ws_part;  // partial states: [CTA][slot 2][Q tile 2][D + 2][128 rows] fp32 (O~, m, l),
+                   // stored column by column so that a warp's accesses are coalesced
+  int* ws_cnt;     // per (item, Q tile, row): K/V tiles accounted for; back to 0 after use
+};
+
+// ----------------------------------------------------------------------------- waits
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicCAS(&g_fa_status, 0, FA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+// Drain wait used on the way out after an abort: ignores the abort flag, still bounded.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicCAS(&g_fa_status, 0, FA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bounded wait: true when the phase of `parity` completed; false when the wait gave up
+// (the status word then holds FA_ERR_TIMEOUT) or another role already gave up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, limit_ns);
+}
+
+struct Item {
+  int bh, q0;
+  int j0, n_kv;    // this piece covers K/V tiles [j0, j0 + n_kv) of the item
+  bool has1;       // the second 128-row tile holds at least one valid query row
+  bool partial;    // the piece covers only part of the item's key range
+  int item;        // linear item index
+  int slot;        // partial-row slot of this CTA: 0 = first piece of its range, 1 = last
+};
+
+// The r-th work item of this CTA. Items are ordered by decreasing cost (causal) and
+// dealt out boustrophedon: CTA b takes b, 2G-1-b, 2G+b, 4G-1-b, ... so that every CTA
+// gets one item from each "row" of G items, alternating heavy and light ends.
+__device__ __forceinline__ int item_of(int r, const Params& p) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int base = r * G;
+  return base + ((r & 1) ? (G - 1 - b) : b);
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ Item decode_item(int t, const Params& p) {
+  Item it;
+  int qblk;
+  if (CAUSAL) {  // heaviest (last) query blocks first
+    qblk = p.n_qblk - 1 - t / p.BH;
+    it.bh = t % p.BH;
+  } else {       // consecutive items share a head's K/V in L2
+    it.bh = t / p.n_qblk;
+    qblk = t % p.n_qblk;
+  }
+  it.q0 = qblk * 2 * BM;
+  it.has1 = it.q0 + BM < p.Nq;
+  if (CAUSAL) {
+    const int last_row = min(it.q0 + 2 * BM, p.Nq) - 1;
+    it.n_kv = min(p.n_kv_all, last_row / BN + 1);
+  } else {
+    it.n_kv = p.n_kv_all;
+  }
+  it.j0 = 0;
+  it.partial = false;
+  it.item = t;
+  it.slot = 0;
+  return it;
+}
+
+// Stream-K range boundaries: CTA c owns units [bound(c), bound(c+1)) of the flattened
+// (item, K/V tile) sequence of W units.
+__device__ __forceinline__ long long sk_bound(long long c, long long W, long long G) {
+  return (c * W) / G;
+}
+// the CTA whose range contains unit u
+__device__ __forceinline__ int sk_owner(long long u, long long W, long long G) {
+  long long c = (u * G) / W;
+  while (c + 1 < G && sk_bound(c + 1, W, G) <= u) ++c;
+  return (int)c;
+}
+
+// Per-thread iterator over this CTA's pieces; every role walks the same sequence.
+struct Sched {
+  long long u, u1;  // stream-K: next unit, end of range
+  int r;            // otherwise: round of the item deal
+  bool first;
+};
+
+__device__ __forceinline__ Sched sched_begin(const Params& p) {
+  Sched s;
+  s.r = 0;
+  s.first = true;
+  s.u = s.u1 = 0;
+  if (p.streamk) {
+    const long long W = (long long)p.n_items * p.n_kv_all;
+    s.u = sk_bound(blockIdx.x, W, gridDim.x);
+    s.u1 = sk_bound(blockIdx.x + 1, W, gridDim.x);
+  }
+  return s;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ bool sched_next(Sched& s, Item& it, const Params& p) {
+  if (!CAUSAL && p.streamk) {
+    if (s.u >= s.u1) return false;
+    const long long n = p.n_kv_all;
+    const int t = (int)(s.u / n);
+    const long long e = min(s.u1, (long long)(t + 1) * n);
+    it = decode_item<false>(t, p);
+    it.j0 = (int)(s.u - (long long)t * n);
+    it.n_kv = (int)(e - s.u);
+    it.partial = it.n_kv != p.n_kv_all;
+    it.slot = s.first ? 0 : 1;
+    s.first = false;
+    s.u = e;
+    return true;
+  }
+  const int t = item_of(s.r, p);
+  if (t >= p.n_items) return false;
+  ++s.r;
+  it = decode_item<CAUSAL>(t, p);
+  return true;
+}
+
+// Maximum of the N values of t as a balanced tree of three-input maxima; t is consumed.
+template <int N>
+__device__ __forceinline__ float tree_max(float* t) {
+  if constexpr (N == 1) {
+    return t[0];
+  } else {
+    constexpr int M = (N + 2) / 3;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const float y = 3 * i + 1 < N ? t[3 * i + 1] : -INFINITY;
+      const float z = 3 * i + 2 < N ? t[3 * i + 2] : -INFINITY;
+      t[i] = max3(t[3 * i], y, z);
+    }
+    return tree_max<M>(t);
+  }
+}
+
+// ----------------------------------------------------------------------------- kernel
+// BF16: type of O (and of Q, K, V unless FP8). FP8: Q, K are E4M3 [BH, N, D] and tmV maps
+// V^T, E4M3 [BH, D, ldvt] (keys contiguous), so that V is a K-major operand of P V.
+template <int D, bool BF16, bool CAUSAL, bool DROP, bool FP8>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+  static_assert(!(FP8 && DROP), "dropout is not combined with E4M3 inputs");
+  static_assert(!FP8 || D == 128, "E4M3 inputs need d = 128 (one 128-byte row per tile row)");
+  using LY = Layout<D, FP8 ? 1 : 2>;
+  constexpr int PART_COLS = D + 2;  // O~[D], m, l of a row, each column stored for 128 rows
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + LY::OFF_BAR);
+  const uint32_t sQ = smem_u32(smem + LY::OFF_Q);
+  const uint32_t sKV = smem_u32(smem + LY::OFF_KV);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars->q_full), 1);
+    mbar_init(smem_u32(&bars->q_empty), 1);
+    for (int s = 0; s < LY::KV_SLOTS; ++s) {
+      mbar_init(smem_u32(&bars->kv_full[s]), 1);
+      mbar_init(smem_u32(&bars->kv_release[s]), 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(smem_u32(&bars->s_full[g]), 1);
+      mbar_init(smem_u32(&bars->p_full[g]), 4);    // one arrival per softmax warp
+      mbar_init(smem_u32(&bars->o_done[g]), 1);
+    }
+    mbar_init(smem_u32(&bars->mma_drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_LOAD && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const unsigned long long lim = p.wait_limit_ns;
+  if (warp >= WARP_LOAD) {
+  regs_dec<REGS_OTHER>();
+  if (warp == WARP_LOAD) {
+    // ======================================================================= producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      // K/V loads are numbered globally (K_0 V_0 K_1 V_1 ... over all items of this CTA);
+      // load i goes to slot i mod KV_SLOTS. The slot's previous occupant (load i - KV_SLOTS)
+      // belongs to release unit u = (i - KV_SLOTS + 1) / 2, whose barrier is kv_release[u mod
+      // KV_SLOTS] at phase u / KV_SLOTS.
+      uint32_t ld = 0, q_ph = 0;
+      uint32_t issued_mask = 0, last_par = 0;  // for draining on abort
+      bool q_issued = false;
+      bool ok = true;
+      auto load_kv = [&](const CUtensorMap* tm, int bh, int row0, bool is_v) -> bool {
+        const uint32_t slot = ld % LY::KV_SLOTS;
+        const uint32_t par = (ld / LY::KV_SLOTS) & 1u;
+        if (ld >= (uint32_t)LY::KV_SLOTS) {
+          const uint32_t u = (ld - LY::KV_SLOTS + 1) >> 1;
+          if (!wait_bar(smem_u32(&bars->kv_release[u % LY::KV_SLOTS]), (u / LY::KV_SLOTS) & 1u,
+                        abort_flag, lim))
+            return false;
+        }
+        const uint32_t full = smem_u32(&bars->kv_full[slot]);
+        mbar_arrive_expect_tx(full, LY::TILE_BYTES);
+        const uint32_t dst = sKV + slot * LY::TILE_BYTES;
+        if (FP8 && is_v) {  // V^T tile: D rows (head dims) x 128 keys starting at key row0
+          tma_load_3d_hint(dst, tm, full, row0, 0, bh, pol_kv);
+        } else {
+#pragma unroll
+          for (int c = 0; c < LY::CHUNKS; ++c)
+            tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, tm, full, c * LY::CHUNK_ELEMS, row0, bh,
+                             pol_kv);
+        }
+        issued_mask |= 1u << slot;
+        last_par = (last_par & ~(1u << slot)) | (par << slot);
+        ++ld;
+        return true;
+      };
+      Sched sch = sched_begin(p);
+      Item it;
+      for (int r = 0; ok && sched_next<CAUSAL>(sch, it, p); ++r) {
+        ok = load_kv(&tmK, it.bh, it.j0 * BN, false);
+        if (!ok) break;
+        ok = wait_bar(smem_u32(&bars->q_empty), q_ph ^ 1, abort_flag, lim);
+        if (!ok) break;
+        q_ph ^= 1;
+        const uint32_t qf = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qf, (it.has1 ? 2 : 1) * LY::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < LY::CHUNKS; ++c)
+          tma_load_3d_hint(sQ + c * LY::CHUNK_BYTES, &tmQ, qf, c * LY::CHUNK_ELEMS, it.q0, it.bh,
+                           pol_q);
+        if (it.has1) {
+#pragma unroll
+          for (int c = 0; c < LY::CHUNKS; ++c)
+            tma_load_3d_hint(sQ + LY::TILE_BYTES + c * LY::CHUNK_BYTES, &tmQ, qf,
+                             c * LY::CHUNK_ELEMS, it.q0 + BM, it.bh, pol_q);
+        }
+        q_issued = true;
+        ok = load_kv(&tmV, it.bh, it.j0 * BN, true);
+        for (int j = 1; j < it.n_kv && ok; ++j) {
+          ok = load_kv(&tmK, it.bh, (it.j0 + j) * BN, false);
+          if (ok) ok = load_kv(&tmV, it.bh, (it.j0 + j) * BN, true);
+        }
+      }
+      if (!ok) {
+        // drain: every issued copy must land before the CTA may exit
+        for (int s = 0; s < LY::KV_SLOTS; ++s)
+          if (issued_mask & (1u << s))
+            wait_drain(smem_u32(&bars->kv_full[s]), (last_par >> s) & 1u, lim);
+        if (q_issued) wait_drain(smem_u32(&bars->q_full), q_ph ^ 1, lim);
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ======================================================================= MMA issuer
+    // The whole warp runs this loop converged, so descriptors and counters stay
+    // warp-uniform; one elected lane issues each tcgen05.mma / commit.
+    {
+      // E4M3: both operands of both products K-major (V^T tiles), type code 0 = E4M3
+      constexpr uint32_t ID_S = umma_idesc_f16(FP8 ? 0 : (BF16 ? 1 : 0), 0, 0, BM, BN);
+      constexpr uint32_t ID_O = umma_idesc_f16(FP8 ? 0 : (BF16 ? 1 : 0), 0, FP8 ? 0 : 1, BM, D);
+      // descriptors are built once; per k-step and per slot only the start-address field
+      // (bits 0-13, in 16-byte units) advances, which never carries out of its field
+      const uint64_t dQ0 = umma_smem_desc(sQ, 16, 1024);
+      const uint64_t dK = umma_smem_desc(sKV, 16, 1024);
+      const uint64_t dV = FP8 ? umma_smem_desc(sKV, 16, 1024) : umma_smem_desc(sKV, LY::CHUNK_BYTES, 1024);
+      uint32_t m = 0;  // global K/V tile counter: K_m is load 2m, V_m is load 2m+1
+      uint32_t q_ph = 0;
+      uint32_t p_ph[2] = {0, 0};
+      bool ok = true;
+      auto wait_all = [&](uint32_t bar, uint32_t par) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
+      };
+      auto kv_wait = [&](uint32_t ld, uint32_t& slot) -> bool {
+        slot = ld % LY::KV_SLOTS;
+        return wait_all(smem_u32(&bars->kv_full[slot]), (ld / LY::KV_SLOTS) & 1u);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (elect_one()) umma_commit(smem_u32(bar));
+        __syncwarp();
+      };
+      // S_g = Q_g K^T : M=128 rows, N=128 keys, K=D (32 bytes per instruction: 16
+      // elements of 16 bits, or 32 of E4M3)
+      auto issue_s = [&](int g, uint32_t kslot) {
+        const uint64_t dq = dQ0 + ((g * LY::TILE_BYTES) >> 4);
+        const uint64_t dk = dK + ((kslot * LY::TILE_BYTES) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int ks = 0; ks < D * (FP8 ? 1 : 2) / 32; ++ks) {
+            const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
+            if constexpr (FP8)
+              umma_ss_f8(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+            else
+              umma_ss(tmem + TMEM_S0 + g * 128, dq + off, dk + off, ID_S, ks > 0 ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+      };
+      // O_g += P_g V : M=128 rows, N=D, K=128 keys; P is read from Tensor Memory
+      // (E4M3: P holds four keys per TMEM column, V^T is K-major: 32 keys per instruction,
+      // 8 TMEM columns and 32 bytes of every V^T row)
+      auto issue_pv = [&](int g, uint32_t vslot, bool acc) {
+        const uint64_t dv = dV + ((vslot * LY::TILE_BYTES) >> 4);
+        if (elect_one()) {
+          if constexpr (FP8) {
+#pragma unroll
+            for (int ks = 0; ks < BN / 32; ++ks)
+              umma_ts_f8(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
+                         dv + ((ks * 32) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks)
+              umma_ts(tmem + TMEM_O0 + g * 128, tmem + TMEM_S0 + g * 128 + ks * 8,
+                      dv + ((ks * 16 * 128) >> 4), ID_O, (acc || ks > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+      };
+      Sched sch = sched_begin(p);
+      Item it;
+      for (int r = 0; ok && sched_next<CAUSAL>(sch, it, p); ++r) {
+        uint32_t sK;
+        ok = kv_wait(2 * m, sK) && wait_all(smem_u32(&bars->q_full), q_ph);
+        if (!ok) break;
+        q_ph ^= 1;
+        tc_fence_after();
+        issue_s(0, sK);
+        commit(&bars->s_full[0]);
+        if (it.has1) {
+          issue_s(1, sK);
+          commit(&bars->s_full[1]);
+        }
+        commit(&bars->kv_release[m % LY::KV_SLOTS]);
+        for (int j = 0; j < it.n_kv; ++j) {
+          const uint32_t mj = m + j;
+          const bool has_next = j + 1 < it.n_kv;
+          uint32_t sV, sKn = 0;
+          ok = kv_wait(2 * mj + 1, sV) && wait_all(smem_u32(&bars->p_full[0]), p_ph[0]);
+          if (!ok) break;
+          p_ph[0] ^= 1;
+          tc_fence_after();
+          issue_pv(0, sV, j > 0);
+          if (has_next) {
+            // S_g(j+1) is issued after PV_g(j): its commit also tells the softmax warps
+            // that O_g is up to date (tcgen05 ops of one thread complete in issue order)
+            ok = kv_wait(2 * mj + 2, sKn);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(0, sKn);
+            commit(&bars->s_full[0]);
+          } else {
+            commit(&bars->o_done[0]);
+          }
+          if (it.has1) {
+            ok = wait_all(smem_u32(&bars->p_full[1]), p_ph[1]);
+            if (!ok) break;
+            p_ph[1] ^= 1;
+            tc_fence_after();
+            issue_pv(1, sV, j > 0);
+            if (has_next) {
+              issue_s(1, sKn);
+              commit(&bars->s_full[1]);
+            } else {
+              commit(&bars->o_done[1]);
+            }
+          }
+          // unit mj+1 = {V_mj, K_mj+1}: both are consumed once the MMAs above complete
+          if (has_next) commit(&bars->kv_release[(mj + 1) % LY::KV_SLOTS]);
+        }
+        m += it.n_kv;
+        if (ok) commit(&bars->q_empty);
+      }
+      // every issued MMA must finish before TMEM can be released
+      commit(&bars->mma_drain);
+      wait_drain(smem_u32(&bars->mma_drain), 0, lim);
+      __syncwarp();
+    }
+  }
+  // exit: every role of the CTA has finished with Tensor Memory
+  tc_fence_before();
+  named_bar_sync(1, NUM_THREADS);
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+  } else {
+    regs_inc<REGS_SOFTMAX>();
+    // ======================================================================= softmax
+    const int g = warp >> 2;         // which Q tile / warpgroup
+    const int wq = warp & 3;         // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;    // row within the tile
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + TMEM_S0 + g * 128;
+    const uint32_t tO = tmem + lane_off + TMEM_O0 + g * 128;
+    const float c = p.c;
+    uint32_t s_ph = 0, o_ph = 0;
+    bool ok = true;
+    Sched sch = sched_begin(p);
+    Item it;
+    for (int rr = 0; ok && sched_next<CAUSAL>(sch, it, p); ++rr) {
+      if (g == 1 && !it.has1) continue;
+      const int row = it.q0 + g * BM + r;
+      const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, kv_lim) visible
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        // dropout: the keep bits of this row for K/V tile j, drawn before S_g(j) is ready
+        // (they do not depend on it), so the generator runs while this warpgroup would
+        // otherwise wait for the tensor core
+        uint32_t kbits[4] = {0, 0, 0, 0};
+        if constexpr (DROP)
+          dropout_row_bits((uint32_t)(it.j0 + j) * (BN / 16), (uint32_t)row, (uint32_t)it.bh,
+                           p.drop_offset, p.drop_keys, p.drop_bias, kbits);
+        // S_g(j) ready; for j > 0 this also means PV_g(j-1) has completed
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full[g]), s_ph, abort_flag, lim));
+        if (!ok) break;
+        s_ph ^= 1;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, sr[q]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) reg_fence(sr[q]);
+
+        const int vis = kv_lim - (it.j0 + j) * BN;
+        const bool full = vis >= BN;
+        auto sv = [&](int k) { return __uint_as_float(sr[k >> 5][k & 31]); };
+        // raw row max over the visible keys: a balanced tree of three-input maxima (depth 5
+        // for 128 keys, against 16 for four running chains)
+        float mt;
+        {
+          float t[43];
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < 42; ++i) t[i] = max3(sv(3 * i), sv(3 * i + 1), sv(3 * i + 2));
+            t[42] = fmaxf(sv(126), sv(127));
+          } else {
+            auto mv = [&](int e) { return e < vis ? sv(e) : -INFINITY; };
+#pragma unroll
+            for (int i = 0; i < 42; ++i) t[i] = max3(mv(3 * i), mv(3 * i + 1), mv(3 * i + 2));
+            t[42] = fmaxf(mv(126), mv(127));
+          }
+          mt = tree_max<43>(t);
+        }
+        const float m_tile = (mt == -INFINITY) ? -INFINITY : mt * c;
+        float m_new = m_run, alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_new = m_tile;
+        } else if (m_tile > m_run + RESCALE_THRESHOLD) {
+          m_new = m_tile;
+          alpha = ex2_approx(m_run - m_new);
+          rescale = true;
+        }
+        const float nb = (m_new == -INFINITY) ? 0.f : -m_new;
+        // P = exp2(S*c - m): the scaling in packed pairs, the exponentials on the MUFU,
+        // the row sum in packed pairs; P is packed to 16-bit pairs (key 2k in the low
+        // half, key 2k+1 in the high half) for the second product
+        const uint64_t c2 = f2(c, c), nb2 = f2(nb, nb);
+        uint64_t acc[4] = {0, 0, 0, 0};
+        uint32_t pk[2][32];
+        // dropout: l keeps the undropped sum; only the 16-bit P of the second product is
+        // masked, pair k by the bits (k & 15, 16 + (k & 15)) of kbits[k >> 4]
+        auto drop_pair = [&](int k, uint32_t w) -> uint32_t {
+          if constexpr (DROP) {
+            return w & pair_mask(kbits[k >> 4], k & 15);
+          } else {
+            return w;
+          }
+        };
+        // P of key pair k (keys 2k, 2k+1) into the packed words of the second product:
+        // two 16-bit values per word, or (E4M3) four 8-bit values per word, lowest key in
+        // the lowest bits; k is a compile-time constant in the unrolled loops below
+        float pe0 = 0.f, pe1 = 0.f;
+        auto emit = [&](int k, float p0, float p1) {
+          if constexpr (FP8) {
+            if ((k & 1) == 0) {
+              pe0 = p0;
+              pe1 = p1;
+            } else {
+              pk[(k >> 1) >> 5][(k >> 1) & 31] = pack4_e4m3(pe0, pe1, p0, p1);
+            }
+          } else {
+            pk[k >> 5][k & 31] = drop_pair(k, pack2<BF16>(p0, p1));
+          }
+        };
+        // two branch-free copies of the loop (full tile / masked tile) so that the
+        // scheduler can overlap the exponentials of many iterations
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            float t0, t1;
+            f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
+            emit(k, p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            float t0, t1;
+            f2_split(f2_fma(f2(sv(2 * k), sv(2 * k + 1)), c2, nb2), t0, t1);
+            const float p0 = 2 * k < vis ? ex2_approx(t0) : 0.f;
+            const float p1 = 2 * k + 1 < vis ? ex2_approx(t1) : 0.f;
+            acc[k & 3] = f2_add(acc[k & 3], f2(p0, p1));
+            emit(k, p0, p1);
+          }
+        }
+        float ls;
+        {
+          float a0, a1, b0, b1;
+          f2_split(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+          (void)b0; (void)b1;
+          ls = a0 + a1;
+        }
+
+        // rescale O~ (in TMEM) when this row's max grew past the threshold
+        if (__any_sync(0xffffffffu, rescale)) {
+          const uint64_t al2 = f2(alpha, alpha);
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float x0, x1;
+              f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2), x0, x1);
+              o[2 * k] = __float_as_uint(x0);
+              o[2 * k + 1] = __float_as_uint(x1);
+            }
+            tmem_st32(tO + q * 32, o);
+          }
+        }
+        l_run = l_run * alpha + ls;
+        m_run = m_new;
+
+        // P overwrites the first 64 (E4M3: 32) columns of this tile's S region (the A
+        // operand of PV)
+        tmem_st32(tS, pk[0]);
+        if constexpr (!FP8) tmem_st32(tS + 32, pk[1]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[g]));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------------ epilogue
+      {
+        const bool w = wait_bar(smem_u32(&bars->o_done[g]), o_ph, abort_flag, lim);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        o_ph ^= 1;
+        tc_fence_after();
+        const bool valid = row < p.Nq;
+        if (!it.partial) {
+          // O = O~ / l (with dropout O~ / (l (1 - p))), L = (m + log2 l) ln 2
+          float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          if constexpr (DROP) inv_l *= p.drop_rscale;
+          if constexpr (FP8) inv_l *= p.o_scale;
+          uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
+                          ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+            uint32_t w16[16];
+            const uint64_t il2 = f2(inv_l, inv_l);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float x0, x1;
+              f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), il2), x0, x1);
+              w16[k] = pack2<BF16>(x0, x1);
+            }
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+            }
+          }
+          if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+          tc_fence_before();
+        } else {
+          // Part of the key range only: keep the state (m, l, O~) of this piece
+          // ("Flash Attention" page, section "平行化": partial states merge with the
+          // associative operator), then the CTA that brings the item's count of merged
+          // K/V tiles to the total merges every piece of the item.
+          float* pcol = p.ws_part + (((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * PART_COLS * BM + r;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + q * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) __stcg(pcol + (q * 32 + k) * BM, __uint_as_float(o[k]));
+          }
+          __stcg(pcol + D * BM, m_run);
+          __stcg(pcol + (D + 1) * BM, l_run);
+          tc_fence_before();
+          // one counter per query row: this thread's row merges independently of the
+          // other rows, so no synchronisation inside the warpgroup is needed
+          __threadfence();
+          int* cnt = p.ws_cnt + ((size_t)it.item * 2 + g) * BM + r;
+          const int before = atomicAdd(cnt, it.n_kv);
+          if (before + it.n_kv == p.n_kv_all) {
+            atomicExch(cnt, 0);  // every piece of this row is in: ready for the next call
+            __threadfence();
+            const long long W = (long long)p.n_items * p.n_kv_all;
+            const long long G = gridDim.x;
+            const long long ub = (long long)it.item * p.n_kv_all;
+            const int c0 = sk_owner(ub, W, G), c1 = sk_owner(ub + p.n_kv_all - 1, W, G);
+            // the first piece is its CTA's last one (slot 1) unless that CTA's range starts
+            // with this item; every later piece is its CTA's first (slot 0)
+            const int slot0 = sk_bound(c0, W, G) < ub ? 1 : 0;
+            auto piece = [&](int cc) -> const float* {
+              return p.ws_part +
+                     (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
+            };
+            float m = -INFINITY;
+            for (int cc = c0; cc <= c1; ++cc) m = fmaxf(m, __ldcg(piece(cc) + D * BM));
+            float l = 0.f;
+            for (int cc = c0; cc <= c1; ++cc) {
+              const float* pc = piece(cc);
+              l += __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
+            }
+            float inv_l = l > 0.f ? 1.f / l : 0.f;
+            if constexpr (DROP) inv_l *= p.drop_rscale;
+            if constexpr (FP8) inv_l *= p.o_scale;
+            uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
+                            ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+#pragma unroll 1
+            for (int q = 0; q < D / 32; ++q) {
+              float acc[32];
+#pragma unroll
+              for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+              for (int cc = c0; cc <= c1; ++cc) {
+                const float* pc = piece(cc);
+                // the chunk's 32 loads are independent: issue them all before the products
+                float x[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) x[k] = __ldcg(pc + (q * 32 + k) * BM);
+                const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = fmaf(x[k], wgt, acc[k]);
+              }
+              if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  dst[v] = make_uint4(pack2<BF16>(acc[8 * v], acc[8 * v + 1]), pack2<BF16>(acc[8 * v + 2], acc[8 * v + 3]),
+                                      pack2<BF16>(acc[8 * v + 4], acc[8 * v + 5]), pack2<BF16>(acc[8 * v + 6], acc[8 * v + 7]));
+              }
+            }
+            if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
+          }
+        }
+      }
+    }
+    // exit: the load/MMA warpgroup releases Tensor Memory after this barrier
+    tc_fence_before();
+    named_bar_sync(1, NUM_THREADS);
+  }
+}
+
+// Bounded-wait self test: one barrier that nothing ever signals.
+__global__ void fa_wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)wait_bar(smem_u32(&bar), 0, &abort_flag, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace fa
