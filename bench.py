@@ -354,6 +354,8 @@ def run_ours(args):
                                  "pct_of_peak": round(100 * w.flops / (ms * 1e-3) / 1e12 / peak, 1),
                                  "ms_min": round(min(per[w.name]), 5), "ms_max": round(max(per[w.name]), 5)}
         cpu = cpu_baseline(budget_s=args.cpu_budget) if (args.cpu_budget > 0 and ws == 1) else None
+        also = secondary_measurements(args) if (ws == 1 and args.also and not (
+            args.fp8 or args.dropout > 0 or args.streamk or args.workloads)) else None
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
@@ -385,11 +387,42 @@ def run_ours(args):
             "gpu_launches": int(launches),
             "wall_s_timed": round(wall_max, 4),
             "cpu_baseline": cpu,
+            "also": also,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def secondary_measurements(args):
+    """The library's other paths, each timed by this script in its own process the same way
+    (L2 flushed before every launch, CUDA events on the launching stream, medians over the
+    steps): the backward pass, dropout forward and backward, E4M3 inputs, and stream-K on the
+    d=64 cross-attention shape next to plain fa_fwd. Not part of the headline metric."""
+    runs = {
+        "bwd": ["--bwd"],
+        "bwd_dropout_0.1": ["--bwd", "--dropout", "0.1"],
+        "fwd_dropout_0.1": ["--dropout", "0.1"],
+        "fwd_fp8_e4m3": ["--fp8"],
+        "fwd_cross_d64_plain": ["--workloads", "b4h12_q1000_k4097_d64_cross"],
+        "fwd_cross_d64_streamk": ["--workloads", "b4h12_q1000_k4097_d64_cross", "--streamk"],
+    }
+    steps = str(max(20, min(args.steps, 100)))
+    out = {}
+    for name, extra in runs.items():
+        cmd = [sys.executable, os.path.abspath(__file__), "--steps", steps, "--warmup", "5",
+               "--cpu-budget", "0", "--no-also", *extra]
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+            line = json.loads(r.stdout.strip().splitlines()[-1])
+            out[name] = {"value": line["value"], "unit": line["unit"],
+                         "entry_point": line["config"].get("entry_point"),
+                         "breakdown": {k: {"ms": v["ms"], "tflops": v["tflops"]}
+                                       for k, v in line.get("breakdown", {}).items()}}
+        except Exception as e:  # a failed side run is reported, never hidden
+            out[name] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
+    return out
 
 
 # ----------------------------------------------------------------------------- backward
@@ -600,6 +633,9 @@ def main():
                     help="time fa_fwd_dropout with this dropout probability (default: no dropout)")
     ap.add_argument("--streamk", action="store_true",
                     help="call fa_fwd_ws with a workspace (stream-K split of full attention)")
+    ap.add_argument("--no-also", dest="also", action="store_false",
+                    help="skip the side measurements of the other paths (backward, dropout, "
+                         "E4M3, stream-K) that a default run adds under 'also'")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of host time for the oracle CPU baseline (0 = skip)")
     args = ap.parse_args()
