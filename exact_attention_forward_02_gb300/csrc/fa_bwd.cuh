@@ -61,6 +61,7 @@ struct BwdBars {
   uint64_t s_full;                      // both score products of the current tile in TMEM
   uint64_t sdp_free;                    // the elementwise warps hold the scores in registers
   uint64_t op_done;                     // the previous tile's accumulating products completed
+  uint64_t pt_full;                     // dK/dV kernel: P^T written back (dV may start)
   uint64_t p_full;                      // 16-bit operands written back to TMEM
   uint64_t done;                        // accumulators final for the current item
   uint64_t mma_drain;
@@ -536,6 +537,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->sdp_free), BW_EW_WARPS);
     mbar_init(smem_u32(&bars->op_done), 1);
+    mbar_init(smem_u32(&bars->pt_full), BW_EW_WARPS);
     mbar_init(smem_u32(&bars->p_full), BW_EW_WARPS);  // one arrival per elementwise warp
     mbar_init(smem_u32(&bars->done), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
@@ -622,7 +624,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint64_t dA = umma_smem_desc(sA, 16, 1024);
     const uint64_t dB = umma_smem_desc(sS, 16, 1024);
     const uint64_t dBmn = umma_smem_desc(sS, LY::CHUNK_BYTES, 1024);
-    uint32_t i_glob = 0, a_ph = 0, p_ph = 0;
+    uint32_t i_glob = 0, a_ph = 0, p_ph = 0, pt_ph = 0;
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t par) {
       return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
@@ -680,18 +682,25 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           tc_fence_after();
           issue_dpt(nslot);
         }
-        ok = wait_all(smem_u32(&bars->p_full), p_ph);
+        const uint64_t dq = dBmn + ((slot * LY::PAIR_BYTES) >> 4);
+        ok = wait_all(smem_u32(&bars->pt_full), pt_ph);
         if (!ok) break;
-        p_ph ^= 1;
+        pt_ph ^= 1;
         tc_fence_after();
         if (elect_one()) {
-          const uint64_t dq = dBmn + ((slot * LY::PAIR_BYTES) >> 4);
           const uint64_t ddo = dq + (LY::TILE_BYTES >> 4);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks) {  // dV += P^T dO_i (K = 128 queries)
             umma_ts(tmem + T_DV, tmem + T_S + ks * 8, ddo + ((ks * 16 * 128) >> 4), ID_G,
                     (i > 0 || ks > 0) ? 1u : 0u);
           }
+        }
+        __syncwarp();
+        ok = wait_all(smem_u32(&bars->p_full), p_ph);
+        if (!ok) break;
+        p_ph ^= 1;
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks) {  // dK += dS^T Q_i
             umma_ts(tmem + T_DK, tmem + T_S + 64 + ks * 8, dq + ((ks * 16 * 128) >> 4), ID_G,
@@ -805,34 +814,65 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             sr[e >> 5][e & 31] = __float_as_uint(
                 hf * 64 + e >= qfirst ? ex2_approx(__uint_as_float(sr[e >> 5][e & 31])) : 0.f);
         }
+        if constexpr (!DROP) {
+          // P^T first, signalled on its own: the dV product needs nothing else and runs
+          // while dS^T = P^T o (dP^T - D) is computed and stored
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pp[16], pd[16];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pp[16];
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + hf * 64 + c * 32 + 2 * kk);
-            const float p0 = __uint_as_float(sr[c][2 * kk]), p1 = __uint_as_float(sr[c][2 * kk + 1]);
-            const uint64_t g2 = f2(__uint_as_float(dr[c][2 * kk]), __uint_as_float(dr[c][2 * kk + 1]));
-            float a0, a1;
-            if constexpr (DROP) {
-              // dV takes P o Z (the 1/(1-p) of Z is applied to dV at the end), dP^T takes Z
+            for (int kk = 0; kk < 16; ++kk)
+              pp[kk] = pack2<BF16>(__uint_as_float(sr[c][2 * kk]), __uint_as_float(sr[c][2 * kk + 1]));
+            tmem_st16(tPT + c * 16, pp);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->pt_full));
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pd[16];
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + hf * 64 + c * 32 + 2 * kk);
+              const uint64_t p2 = f2(__uint_as_float(sr[c][2 * kk]), __uint_as_float(sr[c][2 * kk + 1]));
+              const uint64_t g2 = f2(__uint_as_float(dr[c][2 * kk]), __uint_as_float(dr[c][2 * kk + 1]));
+              float a0, a1;
+              f2_split(f2_mul(p2, f2_add(g2, f2(-dd.x, -dd.y))), a0, a1);
+              pd[kk] = pack2<BF16>(a0, a1);
+            }
+            tmem_st16(tPT + 64 + c * 16, pd);
+          }
+        } else {
+          // under dropout one pass builds both operands (P^T o Z and dS^T = P^T o (dP^T o Z - D),
+          // Z's 1/(1-p) applied to dV at the end): a split pass spills the keep bits and is
+          // slower than the overlap it buys
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pp[16], pd[16];
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const float2 dd = *reinterpret_cast<const float2*>(sLD + 128 + hf * 64 + c * 32 + 2 * kk);
+              const float p0 = __uint_as_float(sr[c][2 * kk]), p1 = __uint_as_float(sr[c][2 * kk + 1]);
+              const uint64_t g2 = f2(__uint_as_float(dr[c][2 * kk]), __uint_as_float(dr[c][2 * kk + 1]));
               const uint32_t z0 = (zb[c] >> (2 * kk)) & 1u, z1 = (zb[c] >> (2 * kk + 1)) & 1u;
+              float a0, a1;
               f2_split(f2_mul(f2(p0, p1), f2_fma(g2, f2(z0 ? p.drop_rscale : 0.f, z1 ? p.drop_rscale : 0.f),
                                                  f2(-dd.x, -dd.y))),
                        a0, a1);
               pp[kk] = pack2<BF16>(z0 ? p0 : 0.f, z1 ? p1 : 0.f);
-            } else {
-              f2_split(f2_mul(f2(p0, p1), f2_add(g2, f2(-dd.x, -dd.y))), a0, a1);
-              pp[kk] = pack2<BF16>(p0, p1);
+              pd[kk] = pack2<BF16>(a0, a1);
             }
-            pd[kk] = pack2<BF16>(a0, a1);
+            tmem_st16(tPT + c * 16, pp);
+            tmem_st16(tPT + 64 + c * 16, pd);
           }
-          tmem_st16(tPT + c * 16, pp);
-          tmem_st16(tPT + 64 + c * 16, pd);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
+        if constexpr (DROP) {
+          if (lane == 0) mbar_arrive(smem_u32(&bars->pt_full));
+        }
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
         named_bar_sync(2, BW_EW_WARPS * 32);  // every thread is done reading sLD
       }
