@@ -724,31 +724,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
           tc_fence_before();
         } else {
-          // Part of the key range only: keep the state (m, l, O~) of this piece
-          // ("Flash Attention" page, section "平行化": partial states merge with the
-          // associative operator), then the CTA that brings the item's count of merged
-          // K/V tiles to the total merges every piece of the item.
-          float* pcol = p.ws_part + (((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * PART_COLS * BM + r;
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld32(tO + q * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) __stcg(pcol + (q * 32 + k) * BM, __uint_as_float(o[k]));
-          }
-          __stcg(pcol + D * BM, m_run);
-          __stcg(pcol + (D + 1) * BM, l_run);
-          tc_fence_before();
-          // one counter per query row: this thread's row merges independently of the
-          // other rows, so no synchronisation inside the warpgroup is needed
-          __threadfence();
+          // Part of the key range only ("Flash Attention" page, section "平行化": partial
+          // states (m, l, O~) merge with the associative operator). A piece that is not the
+          // last of its row stores its state, then adds its K/V tile count to the row's
+          // counter; the piece that completes the count merges. A piece that already finds
+          // every other piece counted skips its own store and merges from Tensor Memory.
+          // One counter per query row: rows merge independently, and tcgen05.ld (a warp-wide
+          // instruction) runs whenever any lane of the warp needs it.
           int* cnt = p.ws_cnt + ((size_t)it.item * 2 + g) * BM + r;
-          const int before = atomicAdd(cnt, it.n_kv);
-          if (before + it.n_kv == p.n_kv_all) {
-            atomicExch(cnt, 0);  // every piece of this row is in: ready for the next call
-            __threadfence();
+          bool merge = ld_acquire_gpu(cnt) + it.n_kv == p.n_kv_all;
+          if (__any_sync(0xffffffffu, !merge)) {
+            float* pcol = p.ws_part + (((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * PART_COLS * BM + r;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t o[32];
+              tmem_ld32(tO + q * 32, o);
+              tmem_wait_ld();
+              reg_fence(o);
+              if (!merge) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) __stcg(pcol + (q * 32 + k) * BM, __uint_as_float(o[k]));
+              }
+            }
+            if (!merge) {
+              __stcg(pcol + D * BM, m_run);
+              __stcg(pcol + (D + 1) * BM, l_run);
+              __threadfence();
+              merge = atomicAdd(cnt, it.n_kv) + it.n_kv == p.n_kv_all;
+            }
+          }
+          if (__any_sync(0xffffffffu, merge)) {
+            if (merge) {
+              atomicExch(cnt, 0);  // every piece of this row is in: ready for the next call
+              __threadfence();
+            }
             const long long W = (long long)p.n_items * p.n_kv_all;
             const long long G = gridDim.x;
             const long long ub = (long long)it.item * p.n_kv_all;
@@ -760,43 +769,102 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               return p.ws_part +
                      (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
             };
-            float m = -INFINITY;
-            for (int cc = c0; cc <= c1; ++cc) m = fmaxf(m, __ldcg(piece(cc) + D * BM));
-            float l = 0.f;
-            for (int cc = c0; cc <= c1; ++cc) {
-              const float* pc = piece(cc);
-              l += __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
-            }
-            float inv_l = l > 0.f ? 1.f / l : 0.f;
-            if constexpr (DROP) inv_l *= p.drop_rscale;
-            if constexpr (FP8) inv_l *= p.o_scale;
+            const int me = blockIdx.x;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
                             ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
-#pragma unroll 1
-            for (int q = 0; q < D / 32; ++q) {
-              float acc[32];
-#pragma unroll
-              for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-              for (int cc = c0; cc <= c1; ++cc) {
-                const float* pc = piece(cc);
-                // the chunk's 32 loads are independent: issue them all before the products
-                float x[32];
-#pragma unroll
-                for (int k = 0; k < 32; ++k) x[k] = __ldcg(pc + (q * 32 + k) * BM);
-                const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) acc[k] = fmaf(x[k], wgt, acc[k]);
-              }
-              if (valid) {
+            const bool out = merge && valid;
+            auto store_chunk = [&](int q, const float (&acc)[32]) {
+              if (out) {
                 uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
                   dst[v] = make_uint4(pack2<BF16>(acc[8 * v], acc[8 * v + 1]), pack2<BF16>(acc[8 * v + 2], acc[8 * v + 3]),
                                       pack2<BF16>(acc[8 * v + 4], acc[8 * v + 5]), pack2<BF16>(acc[8 * v + 6], acc[8 * v + 7]));
               }
+            };
+            // The pieces are combined in the order of their CTAs (c0 first), whichever piece
+            // merges, so that the result does not depend on which one finished last.
+            float m, l;
+            if (c1 - c0 == 1) {
+              // one other piece (an item spans two CTAs): its m, l and the first half of
+              // its O~ are loaded together, the second half while the first is combined
+              const bool first = c0 == me;
+              const float* po = piece(first ? c1 : c0);
+              const float mo = __ldcg(po + D * BM), lo = __ldcg(po + (D + 1) * BM);
+              float x[2][32];
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < 32; ++k) x[h][k] = __ldcg(po + (h * 32 + k) * BM);
+              m = fmaxf(m_run, mo);
+              const float w_own = ex2_approx(m_run - m), w_o = ex2_approx(mo - m);
+              l = first ? l_run * w_own + lo * w_o : lo * w_o + l_run * w_own;
+              const float inv_l = (l > 0.f ? 1.f / l : 0.f) * (DROP ? p.drop_rscale : 1.f) *
+                                  (FP8 ? p.o_scale : 1.f);
+              const float a_own = w_own * inv_l, a_o = w_o * inv_l;
+              const float a0 = first ? a_own : a_o, a1 = first ? a_o : a_own;
+#pragma unroll
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tO + q * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                float acc[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  const float own = __uint_as_float(o[k]);
+                  const float x0 = first ? own : x[q & 1][k], x1 = first ? x[q & 1][k] : own;
+                  acc[k] = fmaf(x1, a1, x0 * a0);
+                }
+                store_chunk(q, acc);
+                if (q + 2 < D / 32) {
+#pragma unroll
+                  for (int k = 0; k < 32; ++k) x[q & 1][k] = __ldcg(po + ((q + 2) * 32 + k) * BM);
+                }
+              }
+            } else {
+              // three or more pieces (short ranges): one chunk of one piece at a time
+              m = m_run;
+              for (int cc = c0; cc <= c1; ++cc)
+                if (cc != me) m = fmaxf(m, __ldcg(piece(cc) + D * BM));
+              l = 0.f;
+              for (int cc = c0; cc <= c1; ++cc) {
+                const float* pc = piece(cc);
+                l += cc == me ? l_run * ex2_approx(m_run - m)
+                              : __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
+              }
+              const float inv_l = (l > 0.f ? 1.f / l : 0.f) * (DROP ? p.drop_rscale : 1.f) *
+                                  (FP8 ? p.o_scale : 1.f);
+              const float a_own = ex2_approx(m_run - m) * inv_l;
+#pragma unroll 1
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tO + q * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                float acc[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+                for (int cc = c0; cc <= c1; ++cc) {
+                  if (cc == me) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[k] = fmaf(__uint_as_float(o[k]), a_own, acc[k]);
+                    continue;
+                  }
+                  const float* pc = piece(cc);
+                  float x[32];
+#pragma unroll
+                  for (int k = 0; k < 32; ++k) x[k] = __ldcg(pc + (q * 32 + k) * BM);
+                  const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
+#pragma unroll
+                  for (int k = 0; k < 32; ++k) acc[k] = fmaf(x[k], wgt, acc[k]);
+                }
+                store_chunk(q, acc);
+              }
             }
-            if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
+            if (out) p.L[(size_t)it.bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
           }
+          tc_fence_before();
         }
       }
     }
