@@ -46,8 +46,9 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [BH, N, d] 16-bit tensor; boxes of 64 elements (128 bytes) x 128 rows x 1 head,
-// 128-byte swizzle; rows past N read as zeros (never the next head's rows).
+// [BH, N, d] 16-bit tensor (Q, K, V loads; O stores); boxes of 64 elements (128 bytes) x
+// 128 rows x 1 head, 128-byte swizzle; rows past N read as zeros and are never written (never
+// the next head's rows).
 int make_map(CUtensorMap* m, const void* base, int d, int N, int BH, bool bf16) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return FA_ERR_TENSOR_MAP;
@@ -119,8 +120,8 @@ int device_info(DeviceInfo** out) {
 }
 
 template <int D, bool BF16, bool CAUSAL, bool DROP, bool FP8 = false>
-int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-           DeviceInfo* di, int grid, cudaStream_t st) {
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+           const CUtensorMap& mo, const Params& p, DeviceInfo* di, int grid, cudaStream_t st) {
   using LY = Layout<D, FP8 ? 1 : 2>;
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL, DROP, FP8>;
   {
@@ -133,12 +134,12 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
       set = true;
     }
   }
-  kern<<<grid, NUM_THREADS, LY::SMEM_BYTES, st>>>(mq, mk, mv, p);
+  kern<<<grid, NUM_THREADS, LY::SMEM_BYTES, st>>>(mq, mk, mv, mo, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// Stream-K workspace: partial rows of every CTA, then per-row counters.
+// Stream-K workspace: partial rows of every CTA, then one counter per (item, Q tile).
 struct WsPlan {
   long long n_items, n_kv, W;
   int G;
@@ -152,7 +153,7 @@ WsPlan ws_plan(long long BH, int Nq, int Nk, int d, int sms) {
   w.G = (int)(w.W < sms ? w.W : sms);
   auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
   w.part_bytes = align((size_t)w.G * 2 * 2 * BM * (d + 4) * sizeof(float));
-  w.cnt_bytes = align((size_t)w.n_items * 2 * BM * sizeof(int));
+  w.cnt_bytes = align((size_t)w.n_items * 2 * sizeof(int));
   w.total = w.part_bytes + w.cnt_bytes;
   return w;
 }
@@ -198,17 +199,18 @@ uint32_t dropout_bias(uint32_t t) { return (0x100u - t) * 0x00010001u; }
 
 template <bool DROP>
 int dispatch(int d, bool bf16, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
-             const CUtensorMap& mv, const Params& p, DeviceInfo* di, int grid, cudaStream_t st) {
+             const CUtensorMap& mv, const CUtensorMap& mo, const Params& p, DeviceInfo* di, int grid,
+             cudaStream_t st) {
   const int key = (d == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
   switch (key) {
-    case 0: return launch<64, false, false, DROP>(mq, mk, mv, p, di, grid, st);
-    case 1: return launch<64, false, true, DROP>(mq, mk, mv, p, di, grid, st);
-    case 2: return launch<64, true, false, DROP>(mq, mk, mv, p, di, grid, st);
-    case 3: return launch<64, true, true, DROP>(mq, mk, mv, p, di, grid, st);
-    case 4: return launch<128, false, false, DROP>(mq, mk, mv, p, di, grid, st);
-    case 5: return launch<128, false, true, DROP>(mq, mk, mv, p, di, grid, st);
-    case 6: return launch<128, true, false, DROP>(mq, mk, mv, p, di, grid, st);
-    default: return launch<128, true, true, DROP>(mq, mk, mv, p, di, grid, st);
+    case 0: return launch<64, false, false, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    case 1: return launch<64, false, true, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    case 2: return launch<64, true, false, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    case 3: return launch<64, true, true, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    case 4: return launch<128, false, false, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    case 5: return launch<128, false, true, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    case 6: return launch<128, true, false, DROP>(mq, mk, mv, mo, p, di, grid, st);
+    default: return launch<128, true, true, DROP>(mq, mk, mv, mo, p, di, grid, st);
   }
 }
 
@@ -264,14 +266,15 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   }
 
   const bool bf16 = dtype == FA_BF16;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((rc = make_map(&mq, Q, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
   if ((rc = make_map(&mk, K, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
   if ((rc = make_map(&mv, V, d, Nk, (int)BH, bf16)) != FA_OK) return rc;
+  if ((rc = make_map(&mo, O, d, Nq, (int)BH, bf16)) != FA_OK) return rc;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return drop ? dispatch<true>(d, bf16, causal, mq, mk, mv, p, di, grid, st)
-              : dispatch<false>(d, bf16, causal, mq, mk, mv, p, di, grid, st);
+  return drop ? dispatch<true>(d, bf16, causal, mq, mk, mv, mo, p, di, grid, st)
+              : dispatch<false>(d, bf16, causal, mq, mk, mv, mo, p, di, grid, st);
 }
 
 // One thread per (row, group of 16 keys): the keep bytes of the dropout mask, computed by
@@ -382,10 +385,11 @@ int run_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int 
   p.drop_keys = philox_keys(0);
   const int grid = p.n_items < di->sms ? p.n_items : di->sms;
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if ((rc = make_map_u8(&mq, Q, d, Nq, (int)BH)) != FA_OK) return rc;
   if ((rc = make_map_u8(&mk, K, d, Nk, (int)BH)) != FA_OK) return rc;
   if ((rc = make_map_vt(&mv, workspace, d, ldvt, (int)BH)) != FA_OK) return rc;
+  if ((rc = make_map(&mo, O, d, Nq, (int)BH, out_dtype == FA_BF16)) != FA_OK) return rc;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const long long kblocks = (ldvt + VT_KEYS - 1) / VT_KEYS;
@@ -397,10 +401,10 @@ int run_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int 
   if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
   const int key = (out_dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
   switch (key) {
-    case 0: return launch<128, false, false, false, true>(mq, mk, mv, p, di, grid, st);
-    case 1: return launch<128, false, true, false, true>(mq, mk, mv, p, di, grid, st);
-    case 2: return launch<128, true, false, false, true>(mq, mk, mv, p, di, grid, st);
-    default: return launch<128, true, true, false, true>(mq, mk, mv, p, di, grid, st);
+    case 0: return launch<128, false, false, false, true>(mq, mk, mv, mo, p, di, grid, st);
+    case 1: return launch<128, false, true, false, true>(mq, mk, mv, mo, p, di, grid, st);
+    case 2: return launch<128, true, false, false, true>(mq, mk, mv, mo, p, di, grid, st);
+    default: return launch<128, true, true, false, true>(mq, mk, mv, mo, p, di, grid, st);
   }
 }
 
@@ -650,7 +654,7 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
   if (w.total > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch)) != FA_OK) return rc;
-  // the per-row counters must start at zero; the array keeps the previous call's contents
+  // the counters must start at zero; the array keeps the previous call's contents
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(reinterpret_cast<uint8_t*>(scratch) + w.part_bytes, 0, w.cnt_bytes, st) !=
       cudaSuccess)

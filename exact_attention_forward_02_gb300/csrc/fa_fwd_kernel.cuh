@@ -21,7 +21,9 @@
 //               tcgen05.mma for S = Q K^T (both operands K-major in shared memory, fp32
 //               accumulator in Tensor Memory) and O~ += P V (P read from Tensor Memory,
 //               V MN-major in shared memory), and signals completion with tcgen05.commit.
-//   warps 10,11 no role (they keep the register split of whole warpgroups).
+//   warps 10,11 store warps, one per Q tile: the softmax warps hand each finished slice of
+//               O (or of a stream-K partial state) over in a shared-memory stage, and the
+//               store warp copies it to global memory with TMA while they go on.
 //   warps 0-7   two softmax warpgroups, one per Q tile (ping-pong): thread r owns query
 //               row r of its tile (TMEM lane r), reads its 128 scores with tcgen05.ld,
 //               applies the mask, keeps (m, l) in registers in base-2 units (the scale is
@@ -51,6 +53,7 @@ constexpr int NUM_WARPS = 12;            // three warpgroups: softmax 0, softmax
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int WARP_LOAD = 8;
 constexpr int WARP_MMA = 9;              // issues every MMA and owns the TMEM allocation
+constexpr int WARP_STORE0 = 10;          // warps 10 and 11: TMA stores of Q tile 0 and 1
 // Register split (launch: 384 threads x 168): the load/MMA warpgroup gives registers
 // to the two softmax warpgroups: 2*128*200 + 128*104 = 64512 = 384*168.
 constexpr uint32_t REGS_SOFTMAX = 200;
@@ -60,6 +63,23 @@ constexpr uint32_t TMEM_S0 = 0, TMEM_O0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O~ only when m grows > 2^8
 constexpr int SMEM_LIMIT = 232448;       // 227 KB opt-in dynamic shared memory per CTA
 constexpr int MAX_SLOTS = 8;
+// Epilogue stage of one Q tile: one 64-column box of O in 16 bits (128 rows x 128 bytes,
+// 128-byte swizzled as the O tensor map expects) or 32 fp32 columns of a partial state.
+constexpr int STAGE_BYTES = 16384;
+enum StageKind : int {
+  STAGE_O_BOX = 0,      // box (x, y, z) of O
+  STAGE_PART = 1,       // `bytes` of a partial state to `dst`
+  STAGE_PART_LAST = 2,  // m and l of a partial state; then count the piece (and merge if last)
+  STAGE_EXIT = 3,       // no more stores
+};
+struct StageCmd {
+  int kind;
+  int x, y, z;     // STAGE_O_BOX: box coordinates (column, row, head); z is also the head
+  float* dst;      // STAGE_PART*: destination
+  uint32_t bytes;
+  int item, n_kv;  // STAGE_PART_LAST: the piece
+  int q0;          //                  and its first query row
+};
 
 struct Barriers {
   uint64_t q_full, q_empty;
@@ -67,6 +87,10 @@ struct Barriers {
   uint64_t kv_release[MAX_SLOTS];  // release unit m = {V of tile m-1, K of tile m}
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t mma_drain;
+  uint64_t stage_full[2], stage_empty[2];  // per Q tile: stage written / copied out
+  uint64_t decided[2];                      // per Q tile: merge_now holds this piece's choice
+  StageCmd cmd[2];
+  int merge_now[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -78,12 +102,13 @@ struct Layout {
   static constexpr int CHUNK_BYTES = BM * 128;        // 128 rows x one 128-byte swizzle span
   static constexpr int CHUNKS = D * ESZ / 128;        // 128-byte spans per row
   static constexpr int CHUNK_ELEMS = 128 / ESZ;       // elements per span
-  static constexpr int FIXED = 2 * TILE_BYTES + 1024 /*align*/ + 512 /*bars*/;
+  static constexpr int FIXED = 2 * TILE_BYTES + 2 * STAGE_BYTES + 1024 /*align*/ + 512 /*bars*/;
   static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TILE_BYTES;
   static constexpr int KV_SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_KV + KV_SLOTS * TILE_BYTES;
+  static constexpr int OFF_STAGE = OFF_KV + KV_SLOTS * TILE_BYTES;  // 1024-byte aligned
+  static constexpr int OFF_BAR = OFF_STAGE + 2 * STAGE_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + (int)sizeof(Barriers) + 1024;
   static_assert(KV_SLOTS >= 2, "need at least two K/V slots");
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
@@ -109,7 +134,7 @@ struct Params {
   int streamk;
   float* ws_part;  // partial states: [CTA][slot 2][Q tile 2][D + 2][128 rows] fp32 (O~, m, l),
                    // stored column by column so that a warp's accesses are coalesced
-  int* ws_cnt;     // per (item, Q tile, row): K/V tiles accounted for; back to 0 after use
+  int* ws_cnt;     // per (item, Q tile): K/V tiles accounted for; back to 0 after use
 };
 
 // ----------------------------------------------------------------------------- waits
@@ -269,7 +294,8 @@ __device__ __forceinline__ float tree_max(float* t) {
 template <int D, bool BF16, bool CAUSAL, bool DROP, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const Params p) {
   static_assert(!(FP8 && DROP), "dropout is not combined with E4M3 inputs");
   static_assert(!FP8 || D == 128, "E4M3 inputs need d = 128 (one 128-byte row per tile row)");
   using LY = Layout<D, FP8 ? 1 : 2>;
@@ -280,6 +306,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   Barriers* bars = reinterpret_cast<Barriers*>(smem + LY::OFF_BAR);
   const uint32_t sQ = smem_u32(smem + LY::OFF_Q);
   const uint32_t sKV = smem_u32(smem + LY::OFF_KV);
+  const uint32_t sStage = smem_u32(smem + LY::OFF_STAGE);
   volatile int* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -296,6 +323,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&bars->s_full[g]), 1);
       mbar_init(smem_u32(&bars->p_full[g]), 4);    // one arrival per softmax warp
       mbar_init(smem_u32(&bars->o_done[g]), 1);
+      mbar_init(smem_u32(&bars->stage_full[g]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&bars->stage_empty[g]), 1);
+      mbar_init(smem_u32(&bars->decided[g]), 1);
     }
     mbar_init(smem_u32(&bars->mma_drain), 1);
     bars->abort_flag = 0;
@@ -305,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == WARP_MMA) {
     tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
@@ -470,6 +501,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           commit(&bars->s_full[1]);
         }
         commit(&bars->kv_release[m % LY::KV_SLOTS]);
+        // Q is read by the S products only: its buffer is free for the next item's Q once
+        // the item's last S products complete, a K/V tile before the item ends
+        if (it.n_kv == 1) commit(&bars->q_empty);
         for (int j = 0; j < it.n_kv; ++j) {
           const uint32_t mj = m + j;
           const bool has_next = j + 1 < it.n_kv;
@@ -505,15 +539,142 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           // unit mj+1 = {V_mj, K_mj+1}: both are consumed once the MMAs above complete
           if (has_next) commit(&bars->kv_release[(mj + 1) % LY::KV_SLOTS]);
+          if (j + 2 == it.n_kv) commit(&bars->q_empty);  // the item's last S products
         }
         m += it.n_kv;
-        if (ok) commit(&bars->q_empty);
       }
       // every issued MMA must finish before TMEM can be released
       commit(&bars->mma_drain);
       wait_drain(smem_u32(&bars->mma_drain), 0, lim);
       __syncwarp();
     }
+  } else {
+    // ======================================================================= store warps
+    // Warp 10 + g copies out what softmax warpgroup g leaves in its stage, one command at a
+    // time: a box of O (TMA tensor store, clipped at the end of the sequence) or a slice of
+    // a partial state (bulk copy). After a partial state's last slice it waits for the
+    // copies to complete, adds the piece's K/V tile count to the tile's counter, and merges
+    // the item's pieces from the workspace if that completed the count.
+    const int g = warp - WARP_STORE0;
+    const uint32_t stg = sStage + g * STAGE_BYTES;
+    // Merge of every piece of (item, Q tile g) from the workspace, four rows per lane. The
+    // arithmetic and its order are those of the softmax warps' merge, so the result does
+    // not depend on which piece completes the count.
+    auto merge_from_workspace = [&](int item, int bh, int q0) {
+      const long long W = (long long)p.n_items * p.n_kv_all;
+      const long long G = gridDim.x;
+      const long long ub = (long long)item * p.n_kv_all;
+      const int c0 = sk_owner(ub, W, G), c1 = sk_owner(ub + p.n_kv_all - 1, W, G);
+      const int slot0 = sk_bound(c0, W, G) < ub ? 1 : 0;
+      const float oscale = (DROP ? p.drop_rscale : 1.f) * (FP8 ? p.o_scale : 1.f);
+#pragma unroll 1
+      for (int rq = 0; rq < BM / 32; ++rq) {
+        const int r = rq * 32 + lane;
+        const int row = q0 + g * BM + r;
+        const bool valid = row < p.Nq;
+        auto piece = [&](int cc) -> const float* {
+          return p.ws_part + (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
+        };
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
+                        ((size_t)bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+        float m, l;
+        if (c1 - c0 == 1) {
+          const float* p0 = piece(c0);
+          const float* p1 = piece(c1);
+          const float m0 = __ldcg(p0 + D * BM), l0 = __ldcg(p0 + (D + 1) * BM);
+          const float m1 = __ldcg(p1 + D * BM), l1 = __ldcg(p1 + (D + 1) * BM);
+          m = fmaxf(m0, m1);
+          const float w0 = ex2_approx(m0 - m), w1 = ex2_approx(m1 - m);
+          l = l0 * w0 + l1 * w1;
+          const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
+          const float a0 = w0 * inv_l, a1 = w1 * inv_l;
+#pragma unroll 1
+          for (int q = 0; q < D / 16; ++q) {
+            float x0[16], x1[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              x0[k] = __ldcg(p0 + (q * 16 + k) * BM);
+              x1[k] = __ldcg(p1 + (q * 16 + k) * BM);
+            }
+            uint32_t w16[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w16[k] = pack2<BF16>(fmaf(x1[2 * k], a1, x0[2 * k] * a0),
+                                   fmaf(x1[2 * k + 1], a1, x0[2 * k + 1] * a0));
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+              dst[0] = make_uint4(w16[0], w16[1], w16[2], w16[3]);
+              dst[1] = make_uint4(w16[4], w16[5], w16[6], w16[7]);
+            }
+          }
+        } else {
+          m = -INFINITY;
+          for (int cc = c0; cc <= c1; ++cc) m = fmaxf(m, __ldcg(piece(cc) + D * BM));
+          l = 0.f;
+          for (int cc = c0; cc <= c1; ++cc) {
+            const float* pc = piece(cc);
+            l += __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
+          }
+          const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
+#pragma unroll 1
+          for (int q = 0; q < D / 16; ++q) {
+            float acc[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+            for (int cc = c0; cc <= c1; ++cc) {
+              const float* pc = piece(cc);
+              const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) acc[k] = fmaf(__ldcg(pc + (q * 16 + k) * BM), wgt, acc[k]);
+            }
+            uint32_t w16[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w16[k] = pack2<BF16>(acc[2 * k], acc[2 * k + 1]);
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+              dst[0] = make_uint4(w16[0], w16[1], w16[2], w16[3]);
+              dst[1] = make_uint4(w16[4], w16[5], w16[6], w16[7]);
+            }
+          }
+        }
+        if (valid) p.L[(size_t)bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
+      }
+    };
+    uint32_t f_ph = 0;
+    while (true) {
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&bars->stage_full[g]), f_ph, abort_flag, lim)))
+        break;
+      f_ph ^= 1;
+      const StageCmd c = bars->cmd[g];
+      if (c.kind == STAGE_EXIT) break;
+      if (lane == 0) {
+        if (c.kind == STAGE_O_BOX)
+          tma_store_3d(&tmO, stg, c.x, c.y, c.z);
+        else
+          bulk_store_s2g(c.dst, stg, c.bytes);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->stage_empty[g]));
+      if (c.kind == STAGE_PART_LAST) {
+        int last = 0;
+        if (lane == 0) {
+          bulk_wait0();  // the piece's whole state is in global memory
+          fence_proxy_async_global();
+          __threadfence();
+          int* cnt = p.ws_cnt + (size_t)c.item * 2 + g;
+          last = atomicAdd(cnt, c.n_kv) + c.n_kv == p.n_kv_all;
+          if (last) {
+            atomicExch(cnt, 0);  // every piece is in: ready for the next call
+            __threadfence();
+          }
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) merge_from_workspace(c.item, c.z, c.q0);
+      }
+    }
+    if (lane == 0) bulk_wait0();  // no copy of this warp is still in flight at exit
+    __syncwarp();
   }
   // exit: every role of the CTA has finished with Tensor Memory
   tc_fence_before();
@@ -533,9 +694,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tO = tmem + lane_off + TMEM_O0 + g * 128;
     const float c = p.c;
     uint32_t s_ph = 0, o_ph = 0;
+    // this tile's epilogue stage: before fill n, the store warp has copied out fill n - 1
+    const uint32_t stg = sStage + g * STAGE_BYTES;
+    uint32_t n_fill = 0, dec_ph = 0;
+    auto stage_acquire = [&]() -> bool {
+      const bool w2 = wait_bar(smem_u32(&bars->stage_empty[g]), (n_fill & 1u) ^ 1u, abort_flag, lim);
+      ++n_fill;
+      return __all_sync(0xffffffffu, w2);
+    };
+    // hand the stage to the store warp; `it` is the current piece
+    Item it = {};
+    auto stage_release = [&](int kind, int x, float* dst, uint32_t bytes) {
+      fence_proxy_async_smem();  // this thread's stage writes -> visible to the TMA copy
+      if (r == 0) {
+        StageCmd& c = bars->cmd[g];
+        c.kind = kind;
+        c.x = x;
+        c.y = it.q0 + g * BM;
+        c.z = it.bh;
+        c.dst = dst;
+        c.bytes = bytes;
+        c.item = it.item;
+        c.n_kv = it.n_kv;
+        c.q0 = it.q0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->stage_full[g]));
+    };
     bool ok = true;
     Sched sch = sched_begin(p);
-    Item it;
     for (int rr = 0; ok && sched_next<CAUSAL>(sch, it, p); ++rr) {
       if (g == 1 && !it.has1) continue;
       const int row = it.q0 + g * BM + r;
@@ -686,6 +873,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) break;
       // ------------------------------------------------------------------ epilogue
+      // O leaves through this tile's shared-memory stage: the warps write one slice (a
+      // 64-column box of 16-bit O, or 32 fp32 columns of a partial state), and the store warp
+      // copies it out with TMA while the warpgroup goes on to its next piece.
       {
         const bool w = wait_bar(smem_u32(&bars->o_done[g]), o_ph, abort_flag, lim);
         ok = __all_sync(0xffffffffu, w);
@@ -693,71 +883,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         o_ph ^= 1;
         tc_fence_after();
         const bool valid = row < p.Nq;
+        // this row's 32 values of box half h (bf16 or fp16 pairs), 128-byte swizzled: the
+        // 16-byte chunk j of row r sits at chunk position j ^ (r mod 8)
+        auto st_box_half = [&](int h, const uint32_t (&w16)[16]) {
+          const uint32_t rowb = stg + (uint32_t)r * 128u;
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st_shared_v4(rowb + ((uint32_t)((4 * h + v) ^ (r & 7)) << 4), w16[4 * v], w16[4 * v + 1],
+                         w16[4 * v + 2], w16[4 * v + 3]);
+        };
         if (!it.partial) {
           // O = O~ / l (with dropout O~ / (l (1 - p))), L = (m + log2 l) ln 2
           float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
           if constexpr (DROP) inv_l *= p.drop_rscale;
           if constexpr (FP8) inv_l *= p.o_scale;
-          uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
-                          ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
+          const uint64_t il2 = f2(inv_l, inv_l);
+          for (int b = 0; b < D / 64; ++b) {
+            ok = stage_acquire();
+            if (!ok) break;
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld32(tO + q * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
-            uint32_t w16[16];
-            const uint64_t il2 = f2(inv_l, inv_l);
+            for (int h = 0; h < 2; ++h) {
+              uint32_t o[32];
+              tmem_ld32(tO + (2 * b + h) * 32, o);
+              tmem_wait_ld();
+              reg_fence(o);
+              uint32_t w16[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              float x0, x1;
-              f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), il2), x0, x1);
-              w16[k] = pack2<BF16>(x0, x1);
+              for (int k = 0; k < 16; ++k) {
+                float x0, x1;
+                f2_split(f2_mul(f2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), il2), x0, x1);
+                w16[k] = pack2<BF16>(x0, x1);
+              }
+              st_box_half(h, w16);
             }
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
-            }
+            stage_release(STAGE_O_BOX, 64 * b, nullptr, 0);
           }
+          if (!ok) break;
           if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
           tc_fence_before();
         } else {
           // Part of the key range only ("Flash Attention" page, section "平行化": partial
-          // states (m, l, O~) merge with the associative operator). A piece that is not the
-          // last of its row stores its state, then adds its K/V tile count to the row's
-          // counter; the piece that completes the count merges. A piece that already finds
-          // every other piece counted skips its own store and merges from Tensor Memory.
-          // One counter per query row: rows merge independently, and tcgen05.ld (a warp-wide
-          // instruction) runs whenever any lane of the warp needs it.
-          int* cnt = p.ws_cnt + ((size_t)it.item * 2 + g) * BM + r;
-          bool merge = ld_acquire_gpu(cnt) + it.n_kv == p.n_kv_all;
-          if (__any_sync(0xffffffffu, !merge)) {
-            float* pcol = p.ws_part + (((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * PART_COLS * BM + r;
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
+          // states (m, l, O~) merge with the associative operator). One counter per (item,
+          // Q tile) holds the K/V tiles of the pieces stored so far. If row 0's thread finds
+          // all other pieces counted, the warpgroup merges at once from its Tensor Memory O~
+          // and its (m, l); otherwise it stores its state through the stage and the store
+          // warp counts the piece (and merges if that completes the count).
+          int* cnt = p.ws_cnt + (size_t)it.item * 2 + g;
+          if (r == 0) {
+            bars->merge_now[g] = ld_acquire_gpu(cnt) + it.n_kv == p.n_kv_all;
+            mbar_arrive(smem_u32(&bars->decided[g]));
+          }
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->decided[g]), dec_ph, abort_flag, lim));
+          if (!ok) break;
+          dec_ph ^= 1;
+          const bool merge = *reinterpret_cast<volatile int*>(&bars->merge_now[g]) != 0;
+          if (!merge) {
+            float* dst = p.ws_part + (((size_t)blockIdx.x * 2 + it.slot) * 2 + g) * PART_COLS * BM;
+            for (int f = 0; f < D / 32; ++f) {
+              ok = stage_acquire();
+              if (!ok) break;
               uint32_t o[32];
-              tmem_ld32(tO + q * 32, o);
+              tmem_ld32(tO + f * 32, o);
               tmem_wait_ld();
               reg_fence(o);
-              if (!merge) {
+              // column-major: column k of the slice holds the 128 rows in order
 #pragma unroll
-                for (int k = 0; k < 32; ++k) __stcg(pcol + (q * 32 + k) * BM, __uint_as_float(o[k]));
-              }
+              for (int k = 0; k < 32; ++k) st_shared_u32(stg + (uint32_t)(k * BM + r) * 4u, o[k]);
+              stage_release(STAGE_PART, 0, dst + f * 32 * BM, 32 * BM * 4);
             }
-            if (!merge) {
-              __stcg(pcol + D * BM, m_run);
-              __stcg(pcol + (D + 1) * BM, l_run);
-              __threadfence();
-              merge = atomicAdd(cnt, it.n_kv) + it.n_kv == p.n_kv_all;
-            }
-          }
-          if (__any_sync(0xffffffffu, merge)) {
-            if (merge) {
-              atomicExch(cnt, 0);  // every piece of this row is in: ready for the next call
-              __threadfence();
-            }
+            if (!ok) break;
+            ok = stage_acquire();
+            if (!ok) break;
+            st_shared_u32(stg + (uint32_t)r * 4u, __float_as_uint(m_run));
+            st_shared_u32(stg + (uint32_t)(BM + r) * 4u, __float_as_uint(l_run));
+            stage_release(STAGE_PART_LAST, 0, dst + D * BM, 2 * BM * 4);
+          } else {
+            if (r == 0) atomicExch(cnt, 0);  // every piece is in: ready for the next call
             const long long W = (long long)p.n_items * p.n_kv_all;
             const long long G = gridDim.x;
             const long long ub = (long long)it.item * p.n_kv_all;
@@ -770,58 +971,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
             };
             const int me = blockIdx.x;
-            uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
-                            ((size_t)it.bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
-            const bool out = merge && valid;
-            auto store_chunk = [&](int q, const float (&acc)[32]) {
-              if (out) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + q * 64);
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                  dst[v] = make_uint4(pack2<BF16>(acc[8 * v], acc[8 * v + 1]), pack2<BF16>(acc[8 * v + 2], acc[8 * v + 3]),
-                                      pack2<BF16>(acc[8 * v + 4], acc[8 * v + 5]), pack2<BF16>(acc[8 * v + 6], acc[8 * v + 7]));
-              }
-            };
+            const float oscale = (DROP ? p.drop_rscale : 1.f) * (FP8 ? p.o_scale : 1.f);
             // The pieces are combined in the order of their CTAs (c0 first), whichever piece
             // merges, so that the result does not depend on which one finished last.
             float m, l;
             if (c1 - c0 == 1) {
               // one other piece (an item spans two CTAs): its m, l and the first half of
-              // its O~ are loaded together, the second half while the first is combined
+              // its O~ are loaded together, the rest while the first half is combined
               const bool first = c0 == me;
               const float* po = piece(first ? c1 : c0);
               const float mo = __ldcg(po + D * BM), lo = __ldcg(po + (D + 1) * BM);
               float x[2][32];
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
+              for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int k = 0; k < 32; ++k) x[h][k] = __ldcg(po + (h * 32 + k) * BM);
+                for (int k = 0; k < 32; ++k) x[hh][k] = __ldcg(po + (hh * 32 + k) * BM);
               m = fmaxf(m_run, mo);
               const float w_own = ex2_approx(m_run - m), w_o = ex2_approx(mo - m);
               l = first ? l_run * w_own + lo * w_o : lo * w_o + l_run * w_own;
-              const float inv_l = (l > 0.f ? 1.f / l : 0.f) * (DROP ? p.drop_rscale : 1.f) *
-                                  (FP8 ? p.o_scale : 1.f);
+              const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
               const float a_own = w_own * inv_l, a_o = w_o * inv_l;
               const float a0 = first ? a_own : a_o, a1 = first ? a_o : a_own;
+              for (int b = 0; b < D / 64; ++b) {
+                ok = stage_acquire();
+                if (!ok) break;
 #pragma unroll
-              for (int q = 0; q < D / 32; ++q) {
-                uint32_t o[32];
-                tmem_ld32(tO + q * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
-                float acc[32];
+                for (int h = 0; h < 2; ++h) {
+                  const int q = 2 * b + h;
+                  uint32_t o[32];
+                  tmem_ld32(tO + q * 32, o);
+                  tmem_wait_ld();
+                  reg_fence(o);
+                  uint32_t w16[16];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                  const float own = __uint_as_float(o[k]);
-                  const float x0 = first ? own : x[q & 1][k], x1 = first ? x[q & 1][k] : own;
-                  acc[k] = fmaf(x1, a1, x0 * a0);
+                  for (int k = 0; k < 16; ++k) {
+                    float acc2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                      const float own = __uint_as_float(o[2 * k + e]);
+                      const float xo = x[h][2 * k + e];
+                      const float x0 = first ? own : xo, x1 = first ? xo : own;
+                      acc2[e] = fmaf(x1, a1, x0 * a0);
+                    }
+                    w16[k] = pack2<BF16>(acc2[0], acc2[1]);
+                  }
+                  st_box_half(h, w16);
+                  if (q + 2 < D / 32) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) x[h][k] = __ldcg(po + ((q + 2) * 32 + k) * BM);
+                  }
                 }
-                store_chunk(q, acc);
-                if (q + 2 < D / 32) {
-#pragma unroll
-                  for (int k = 0; k < 32; ++k) x[q & 1][k] = __ldcg(po + ((q + 2) * 32 + k) * BM);
-                }
+                stage_release(STAGE_O_BOX, 64 * b, nullptr, 0);
               }
+              if (!ok) break;
             } else {
               // three or more pieces (short ranges): one chunk of one piece at a time
               m = m_run;
@@ -833,41 +1035,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 l += cc == me ? l_run * ex2_approx(m_run - m)
                               : __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
               }
-              const float inv_l = (l > 0.f ? 1.f / l : 0.f) * (DROP ? p.drop_rscale : 1.f) *
-                                  (FP8 ? p.o_scale : 1.f);
+              const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
               const float a_own = ex2_approx(m_run - m) * inv_l;
-#pragma unroll 1
-              for (int q = 0; q < D / 32; ++q) {
-                uint32_t o[32];
-                tmem_ld32(tO + q * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
-                float acc[32];
+              for (int b = 0; b < D / 64; ++b) {
+                ok = stage_acquire();
+                if (!ok) break;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-                for (int cc = c0; cc <= c1; ++cc) {
-                  if (cc == me) {
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t o[32];
+                  tmem_ld32(tO + (2 * b + h) * 32, o);
+                  tmem_wait_ld();
+                  reg_fence(o);
+                  float acc[32];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[k] = fmaf(__uint_as_float(o[k]), a_own, acc[k]);
-                    continue;
+                  for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+                  for (int cc = c0; cc <= c1; ++cc) {
+                    if (cc == me) {
+#pragma unroll
+                      for (int k = 0; k < 32; ++k) acc[k] = fmaf(__uint_as_float(o[k]), a_own, acc[k]);
+                      continue;
+                    }
+                    const float* pc = piece(cc);
+                    float xx[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) xx[k] = __ldcg(pc + ((2 * b + h) * 32 + k) * BM);
+                    const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[k] = fmaf(xx[k], wgt, acc[k]);
                   }
-                  const float* pc = piece(cc);
-                  float x[32];
+                  uint32_t w16[16];
 #pragma unroll
-                  for (int k = 0; k < 32; ++k) x[k] = __ldcg(pc + (q * 32 + k) * BM);
-                  const float wgt = ex2_approx(__ldcg(pc + D * BM) - m) * inv_l;
-#pragma unroll
-                  for (int k = 0; k < 32; ++k) acc[k] = fmaf(x[k], wgt, acc[k]);
+                  for (int k = 0; k < 16; ++k) w16[k] = pack2<BF16>(acc[2 * k], acc[2 * k + 1]);
+                  st_box_half(h, w16);
                 }
-                store_chunk(q, acc);
+                stage_release(STAGE_O_BOX, 64 * b, nullptr, 0);
               }
+              if (!ok) break;
             }
-            if (out) p.L[(size_t)it.bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
+            if (valid) p.L[(size_t)it.bh * p.Nq + row] = (m + log2f(l)) * 0.69314718055994531f;
           }
           tc_fence_before();
         }
       }
     }
+    // the store warp of this tile stops after the copies handed to it so far
+    if (ok && stage_acquire()) stage_release(STAGE_EXIT, 0, nullptr, 0);
     // exit: the load/MMA warpgroup releases Tensor Memory after this barrier
     tc_fence_before();
     named_bar_sync(1, NUM_THREADS);

@@ -86,8 +86,10 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
  * attention split the key range of work items across CTAs so that every SM gets the same
  * number of K/V tiles ("stream-K"): a CTA that covers only part of an item's keys stores
  * the item rows' partial state (m, l, unnormalised O) in the workspace; the CTA that
- * completes a row's key range merges the partial states with the associative combine of
- * the online softmax ("Flash Attention" page, section "平行化") and writes O and L.
+ * completes a query tile's key range merges the partial states with the associative
+ * combine of the online softmax ("Flash Attention" page, section "平行化") and writes O and
+ * L. The partial states are combined in a fixed order, so results do not depend on which
+ * CTA finishes last.
  * Same arguments, layout and results as fa_fwd (up to rounding order), plus:
  *   workspace       device pointer, 256-byte aligned, at least fa_fwd_workspace_bytes()
  *                   bytes, ZERO-FILLED before its first use; every completed call leaves
