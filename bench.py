@@ -203,9 +203,11 @@ def run_ours(args):
             fp8ws[w.name] = torch.empty(fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.Nk, w.d),
                                         dtype=torch.uint8, device=dev)
         L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
-        # stream-K workspace for full attention (zero-filled once; calls keep it zeroed),
-        # only when --streamk asks for it
-        nws = fa.fa_fwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, w.causal) if args.streamk else 0
+        # stream-K workspace for full attention (zero-filled once; calls keep it zeroed):
+        # --sched auto calls fa_fwd_ws wherever the library asks for one (full attention
+        # whose work items do not fill whole waves of SMs), --sched plain calls fa_fwd
+        nws = (fa.fa_fwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, w.causal)
+               if args.sched != "plain" and w.dtype != gen.FP8 and args.dropout == 0 else 0)
         wsp = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev) if nws else None
         devbuf[w.name] = (qd, kd, vd, O, L, wsp)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -288,7 +290,7 @@ def run_ours(args):
                         torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()) for w in wl}
     h2d = sum(t.numel() * t.element_size() for w in wl for t in host[w.name])
     d2h = sum(t.numel() * t.element_size() for w in wl for t in pin_out[w.name])
-    use_host_api = not (args.fp8 or args.dropout > 0 or args.streamk)
+    use_host_api = not (args.fp8 or args.dropout > 0)
     host_ws = {}
     if use_host_api:
         for w in wl:
@@ -355,7 +357,12 @@ def run_ours(args):
                                  "ms_min": round(min(per[w.name]), 5), "ms_max": round(max(per[w.name]), 5)}
         cpu = cpu_baseline(budget_s=args.cpu_budget) if (args.cpu_budget > 0 and ws == 1) else None
         also = secondary_measurements(args) if (ws == 1 and args.also and not (
-            args.fp8 or args.dropout > 0 or args.streamk or args.workloads)) else None
+            args.fp8 or args.dropout > 0 or args.sched != "auto" or args.workloads)) else None
+        entry = {w.name: ("fa_fwd_fp8 (V^T transpose + attention kernel)" if w.dtype == gen.FP8 else
+                          "fa_fwd_dropout" if args.dropout > 0 else
+                          "fa_fwd" if devbuf[w.name][5] is None else
+                          "fa_fwd_ws (stream-K split of the key range, caller workspace)")
+                 for w in wl}
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
@@ -365,9 +372,8 @@ def run_ours(args):
                        "shapes": [w.describe() for w in wl],
                        "l2": "flushed before every launch (256 MiB write, outside the events)",
                        "parallelism": "replicas" if ws > 1 else "single GPU",
-                       "entry_point": ("fa_fwd_fp8 (V^T transpose + attention kernel)" if args.fp8 else
-                                       "fa_fwd_dropout" if args.dropout > 0 else
-                                       "fa_fwd_ws (stream-K)" if args.streamk else "fa_fwd"),
+                       "entry_point": entry,
+                       "sched": args.sched,
                        "dropout": args.dropout,
                        "pct_of_peak": round(100 * value / ws / peak, 1)},
             "breakdown": breakdown,
@@ -398,15 +404,17 @@ def run_ours(args):
 def secondary_measurements(args):
     """The library's other paths, each timed by this script in its own process the same way
     (L2 flushed before every launch, CUDA events on the launching stream, medians over the
-    steps): the backward pass, dropout forward and backward, E4M3 inputs, and stream-K on the
-    d=64 cross-attention shape next to plain fa_fwd. Not part of the headline metric."""
+    steps): the backward pass, dropout forward and backward, E4M3 inputs, plain fa_fwd (no
+    stream-K) on the full N=4096 workload, and the d=64 cross-attention shape with and
+    without stream-K. Not part of the headline metric."""
     runs = {
         "bwd": ["--bwd"],
         "bwd_dropout_0.1": ["--bwd", "--dropout", "0.1"],
         "fwd_dropout_0.1": ["--dropout", "0.1"],
         "fwd_fp8_e4m3": ["--fp8"],
-        "fwd_cross_d64_plain": ["--workloads", "b4h12_q1000_k4097_d64_cross"],
-        "fwd_cross_d64_streamk": ["--workloads", "b4h12_q1000_k4097_d64_cross", "--streamk"],
+        "fwd_full_n4096_plain_fa_fwd": ["--workloads", "b2h8_n4096_d128_full", "--sched", "plain"],
+        "fwd_cross_d64_plain": ["--workloads", "b4h12_q1000_k4097_d64_cross", "--sched", "plain"],
+        "fwd_cross_d64_streamk": ["--workloads", "b4h12_q1000_k4097_d64_cross", "--sched", "auto"],
     }
     steps = str(max(20, min(args.steps, 100)))
     out = {}
@@ -631,8 +639,10 @@ def main():
                     help="time fa_fwd_fp8 on the E4M3 versions of the two d=128 workloads")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="time fa_fwd_dropout with this dropout probability (default: no dropout)")
-    ap.add_argument("--streamk", action="store_true",
-                    help="call fa_fwd_ws with a workspace (stream-K split of full attention)")
+    ap.add_argument("--sched", choices=("auto", "plain"), default="auto",
+                    help="auto (default): fa_fwd_ws with a workspace wherever the library's "
+                         "stream-K split applies (full attention whose work items do not fill "
+                         "whole waves of SMs), fa_fwd elsewhere; plain: fa_fwd only")
     ap.add_argument("--no-also", dest="also", action="store_false",
                     help="skip the side measurements of the other paths (backward, dropout, "
                          "E4M3, stream-K) that a default run adds under 'also'")
