@@ -175,6 +175,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 struct Item {
   int bh, q0;
   int j0, n_kv;    // this piece covers K/V tiles [j0, j0 + n_kv) of the item
+  int n_kv0;       // of which the first n_kv0 reach Q tile 0 (causal: one fewer, the last
+                   // tile lies wholly above tile 0's diagonal)
   bool has1;       // the second 128-row tile holds at least one valid query row
   bool partial;    // the piece covers only part of the item's key range
   int item;        // linear item index
@@ -206,8 +208,11 @@ __device__ __forceinline__ Item decode_item(int t, const Params& p) {
   if (CAUSAL) {
     const int last_row = min(it.q0 + 2 * BM, p.Nq) - 1;
     it.n_kv = min(p.n_kv_all, last_row / BN + 1);
+    const int last_row0 = min(it.q0 + BM, p.Nq) - 1;
+    it.n_kv0 = min(p.n_kv_all, last_row0 / BN + 1);
   } else {
     it.n_kv = p.n_kv_all;
+    it.n_kv0 = it.n_kv;
   }
   it.j0 = 0;
   it.partial = false;
@@ -258,6 +263,7 @@ __device__ __forceinline__ bool sched_next(Sched& s, Item& it, const Params& p) 
     it = decode_item<false>(t, p);
     it.j0 = (int)(s.u - (long long)t * n);
     it.n_kv = (int)(e - s.u);
+    it.n_kv0 = it.n_kv;
     it.partial = it.n_kv != p.n_kv_all;
     it.slot = s.first ? 0 : 1;
     s.first = false;
@@ -508,21 +514,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t mj = m + j;
           const bool has_next = j + 1 < it.n_kv;
           uint32_t sV, sKn = 0;
-          ok = kv_wait(2 * mj + 1, sV) && wait_all(smem_u32(&bars->p_full[0]), p_ph[0]);
-          if (!ok) break;
-          p_ph[0] ^= 1;
-          tc_fence_after();
-          issue_pv(0, sV, j > 0);
-          if (has_next) {
-            // S_g(j+1) is issued after PV_g(j): its commit also tells the softmax warps
-            // that O_g is up to date (tcgen05 ops of one thread complete in issue order)
-            ok = kv_wait(2 * mj + 2, sKn);
+          bool have_kn = false;
+          auto wait_kn = [&]() -> bool {  // K_(j+1), before the first S product that reads it
+            if (!have_kn) {
+              if (!kv_wait(2 * mj + 2, sKn)) return false;
+              have_kn = true;
+              tc_fence_after();
+            }
+            return true;
+          };
+          if (j < it.n_kv0) {
+            ok = kv_wait(2 * mj + 1, sV) && wait_all(smem_u32(&bars->p_full[0]), p_ph[0]);
             if (!ok) break;
+            p_ph[0] ^= 1;
             tc_fence_after();
-            issue_s(0, sKn);
-            commit(&bars->s_full[0]);
+            issue_pv(0, sV, j > 0);
+            if (j + 1 < it.n_kv0) {
+              // S_g(j+1) is issued after PV_g(j): its commit also tells the softmax warps
+              // that O_g is up to date (tcgen05 ops of one thread complete in issue order)
+              ok = wait_kn();
+              if (!ok) break;
+              issue_s(0, sKn);
+              commit(&bars->s_full[0]);
+            } else {
+              commit(&bars->o_done[0]);
+            }
           } else {
-            commit(&bars->o_done[0]);
+            ok = kv_wait(2 * mj + 1, sV);
+            if (!ok) break;
           }
           if (it.has1) {
             ok = wait_all(smem_u32(&bars->p_full[1]), p_ph[1]);
@@ -531,6 +550,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             issue_pv(1, sV, j > 0);
             if (has_next) {
+              ok = wait_kn();
+              if (!ok) break;
               issue_s(1, sKn);
               commit(&bars->s_full[1]);
             } else {
@@ -728,7 +749,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = it.q0 + g * BM + r;
       const int kv_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, kv_lim) visible
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < it.n_kv; ++j) {
+      const int n_kv_g = g == 0 ? it.n_kv0 : it.n_kv;  // K/V tiles that reach this Q tile
+      for (int j = 0; j < n_kv_g; ++j) {
         // dropout: the keep bits of this row for K/V tile j, drawn before S_g(j) is ready
         // (they do not depend on it), so the generator runs while this warpgroup would
         // otherwise wait for the tensor core
