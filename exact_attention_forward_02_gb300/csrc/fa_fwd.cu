@@ -487,7 +487,11 @@ int noalloc_scratch(void** out) {
 // once), and one stream per slot runs the slot's attention launches; per-slot events
 // chain them: inputs in -> launch -> outputs out -> slot free for the next chunk.
 constexpr int HOST_SLOTS = 4;
-constexpr int HOST_CHUNKS = 8;  // chunks per call when there are enough heads
+// Heads per chunk: enough for copies of at least 8 MB per tensor where the problem has the
+// heads (measured on the GB300's host link with the other direction busy: 134 GB/s for 2 MB
+// copies, 169 for 4 MB, 175 for 8 MB, 183 for 16 MB). The last chunk takes a quarter of
+// that, so that what follows the last copy-in (its attention and its copy-out) is short.
+constexpr size_t HOST_COPY_TARGET = 8u << 20;
 
 struct HostPipe {
   bool ok = false;
@@ -516,20 +520,31 @@ int host_pipe(int dev, HostPipe** out) {
 }
 
 struct HostChunks {
-  long long hc, n;             // heads per chunk, number of chunks
+  long long hc, hc_tail, n;    // heads per chunk (slot capacity), of the last chunk; chunks
   size_t q, kv, o, l;          // bytes per head of Q (and O), of K (and V), of O, of L
   size_t off_k, off_v, off_o, off_l, slot;  // layout of one slot
   int slots;
 };
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+// Heads of the chunk that starts with `rem` heads left: full chunks, then the last full
+// chunk shortened so that the final one has hc_tail heads.
+long long chunk_heads(long long rem, const HostChunks& c) {
+  if (rem <= c.hc_tail) return rem;
+  if (rem <= c.hc + c.hc_tail) return rem - c.hc_tail;
+  return c.hc;
+}
 HostChunks host_chunks(long long BH, int Nq, int Nk, int d) {
   HostChunks c;
-  c.hc = (BH + HOST_CHUNKS - 1) / HOST_CHUNKS;
-  c.n = (BH + c.hc - 1) / c.hc;
   c.q = (size_t)Nq * d * 2;
   c.kv = (size_t)Nk * d * 2;
   c.o = c.q;
   c.l = (size_t)Nq * 4;
+  const size_t per_head = c.q < c.kv ? c.q : c.kv;
+  c.hc = (long long)((HOST_COPY_TARGET + per_head - 1) / per_head);
+  if (c.hc > BH) c.hc = BH;
+  c.hc_tail = c.hc / 4 > 1 ? c.hc / 4 : 1;
+  c.n = 0;
+  for (long long h0 = 0; h0 < BH; h0 += chunk_heads(BH - h0, c)) ++c.n;
   c.off_k = align256(c.hc * c.q);
   c.off_v = c.off_k + align256(c.hc * c.kv);
   c.off_o = c.off_v + align256(c.hc * c.kv);
@@ -579,11 +594,11 @@ int fa_fwd_host(const void* Q, const void* K, const void* V, void* O, float* L, 
   const uint8_t* hv = static_cast<const uint8_t*>(V);
   uint8_t* ho = static_cast<uint8_t*>(O);
   uint8_t* hl = reinterpret_cast<uint8_t*>(L);
-  for (long long ch = 0; ch < c.n; ++ch) {
+  long long h0 = 0;
+  for (long long ch = 0; ch < c.n; ++ch, h0 += chunk_heads(BH - h0, c)) {
     const int s = (int)(ch % c.slots);
     uint8_t* base = static_cast<uint8_t*>(workspace) + (size_t)s * c.slot;
-    const long long h0 = ch * c.hc;
-    const long long nh = (BH - h0) < c.hc ? (BH - h0) : c.hc;
+    const long long nh = chunk_heads(BH - h0, c);
     // inputs: once the slot's previous chunk has left it
     if (ch >= c.slots && !ok(cudaStreamWaitEvent(hp->h2d, hp->freed[s], 0))) return FA_ERR_CUDA;
     if (!ok(cudaMemcpyAsync(base, hq + h0 * c.q, nh * c.q, cudaMemcpyHostToDevice, hp->h2d)) ||

@@ -131,8 +131,9 @@ int fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* 
 
 /* fa_fwd_host -- fa_fwd on HOST buffers: Q, K, V are read from and O, L written to host
  * memory, with the copies overlapped with the computation.
- * The heads are processed in up to 8 chunks that stream through a ring of up to 4 device
- * slots in `workspace`. Library streams carry the work: one takes every host-to-device
+ * The heads are processed in chunks that stream through a ring of up to 4 device slots in
+ * `workspace`: chunks of enough heads for copies of at least 8 MB per tensor (where there
+ * are that many heads), the last one a quarter of that size. Library streams carry the work: one takes every host-to-device
  * copy, one every device-to-host copy (so both directions run at once), and each slot
  * has one for its attention launches. Events chain them per slot: inputs in, launch,
  * outputs out, slot free for the next chunk.

@@ -135,6 +135,10 @@ def test_host_buffer_api_host_checks():
     assert fa.fa_fwd_host(*base, P + 16, need, None) == fa.FA_ERR_ALIGN
     assert fa.fa_fwd_host(0, *base[1:], P, need, None) == fa.FA_ERR_NULL
     assert fa.fa_fwd_host(*base[:9], 96, *base[10:], P, need, None) == fa.FA_ERR_HEAD_DIM
-    # more heads than chunks: several heads per chunk, at most four slots
-    assert fa.fa_fwd_host_workspace_bytes(2, 8, 4096, 4096, 128) == 4 * (
-        2 * (4096 * 128 * 2) * 4 + ((2 * 4096 * 4 + 255) // 256) * 256)
+    # 1 MiB per head and tensor: chunks of 8 heads (8 MiB copies), the last one of 2, so
+    # 16 heads run as 8 + 6 + 2 through three slots of 8 heads each (Q, K, V, O and L)
+    assert fa.fa_fwd_host_workspace_bytes(2, 8, 4096, 4096, 128) == 3 * (
+        8 * (4096 * 128 * 2) * 4 + ((8 * 4096 * 4 + 255) // 256) * 256)
+    # 8 MiB per head and tensor: one head per chunk, four slots
+    assert fa.fa_fwd_host_workspace_bytes(1, 6, 32768, 32768, 128) == 4 * (
+        (32768 * 128 * 2) * 4 + 32768 * 4)

@@ -40,12 +40,16 @@ def run_host(w, q, k, v, pinned=True):
     return O, L
 
 
+# Chunks hold enough heads for 8 MiB per tensor (the smaller of Q and K), capped at the
+# head count; the last chunk has a quarter of that (at least one head).
 CASES = [
-    (1, 1, 128, 128, 64, gen.F16, False),
-    (2, 3, 300, 257, 64, gen.F16, True),        # 6 heads: chunks of one head
-    (2, 8, 1000, 1000, 128, gen.BF16, True),    # 16 heads: 8 chunks of 2 through 4 slots
-    (3, 7, 257, 600, 128, gen.BF16, False),     # 21 heads: chunks of 3, the last one full
-    (1, 13, 129, 131, 64, gen.F16, False),      # 13 heads: a short last chunk
+    (1, 1, 128, 128, 64, gen.F16, False),       # one chunk of one head
+    (2, 3, 300, 257, 64, gen.F16, True),        # small heads: 5 + 1
+    (2, 8, 1000, 1000, 128, gen.BF16, True),    # 12 + 4
+    (3, 7, 257, 600, 128, gen.BF16, False),     # 16 + 5
+    (1, 13, 129, 131, 64, gen.F16, False),      # 10 + 3
+    (3, 7, 8192, 8192, 128, gen.BF16, True),    # 2 MiB heads: 4 4 4 4 4 1, the 4-slot ring wraps
+    (1, 6, 8192, 4096, 128, gen.BF16, False),   # 1 MiB K/V heads: 5 + 1
 ]
 
 
