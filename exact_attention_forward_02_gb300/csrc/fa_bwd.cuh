@@ -62,6 +62,7 @@ struct BwdBars {
   uint64_t sdp_free;                    // the elementwise warps hold the scores in registers
   uint64_t op_done;                     // the previous tile's accumulating products completed
   uint64_t pt_full;                     // dK/dV kernel: P^T written back (dV may start)
+  uint64_t dp_full, dp_read;            // dK/dV kernel: dP^T computed / read by every EW warp
   uint64_t p_full;                      // 16-bit operands written back to TMEM
   uint64_t done;                        // accumulators final for the current item
   uint64_t mma_drain;
@@ -509,15 +510,18 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
 // ============================================================================ dK, dV kernel
 // CTA item: (bh, key tile kt). Streams Q_i, dO_i; per query tile:
-//   S^T = K Q_i^T, dP^T = V dO_i^T  (TMEM)  ->  P^T, dS^T (16-bit, over them)
+//   S^T = K Q_i^T, dP^T = V dO_i^T  (TMEM)  ->  P^T, dS^T (16-bit, over S^T)
 //   ->  dV += P^T dO_i,  dK += dS^T Q_i
+// TMEM: two 128-column score regions that swap roles every query tile, then dK and dV.
 template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     fa_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                       const BwdParams p) {
   using LY = BwdLayout<D>;
-  constexpr uint32_t T_S = 0, T_DP = 128, T_DK = 256, T_DV = 256 + D, T_COLS = 512;
+  // score regions [0, 128) and [128, 256): query tile g (counted over the CTA's items)
+  // takes S^T in region g & 1 and dP^T in the other one
+  constexpr uint32_t T_DK = 256, T_DV = 256 + D, T_COLS = 512;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + LY::OFF_BAR);
@@ -535,9 +539,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       mbar_init(smem_u32(&bars->release[s]), 1);
     }
     mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->sdp_free), BW_EW_WARPS);
     mbar_init(smem_u32(&bars->op_done), 1);
     mbar_init(smem_u32(&bars->pt_full), BW_EW_WARPS);
+    mbar_init(smem_u32(&bars->dp_full), 1);
+    mbar_init(smem_u32(&bars->dp_read), BW_EW_WARPS);
     mbar_init(smem_u32(&bars->p_full), BW_EW_WARPS);  // one arrival per elementwise warp
     mbar_init(smem_u32(&bars->done), 1);
     mbar_init(smem_u32(&bars->mma_drain), 1);
@@ -624,40 +629,47 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint64_t dA = umma_smem_desc(sA, 16, 1024);
     const uint64_t dB = umma_smem_desc(sS, 16, 1024);
     const uint64_t dBmn = umma_smem_desc(sS, LY::CHUNK_BYTES, 1024);
-    uint32_t i_glob = 0, a_ph = 0, p_ph = 0, pt_ph = 0;
+    uint32_t i_glob = 0, a_ph = 0, p_ph = 0, pt_ph = 0, r_ph = 0;
     bool ok = true;
     auto wait_all = [&](uint32_t bar, uint32_t par) {
       return __all_sync(0xffffffffu, wait_bar(bar, par, abort_flag, lim));
     };
-    // S^T = K Q_i^T into T_S, dP^T = V dO_i^T into T_DP (K = D per product)
-    auto issue_dpt = [&](uint32_t slot) {
+    // dP^T = V dO_i^T into score region `reg` (K = D per product)
+    auto issue_dpt = [&](uint32_t slot, uint32_t reg) {
       if (elect_one()) {
         const uint64_t ddo = dB + ((slot * LY::PAIR_BYTES) >> 4) + (LY::TILE_BYTES >> 4);
         const uint64_t dv = dA + (LY::TILE_BYTES >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
-          umma_ss(tmem + T_DP, dv + off, ddo + off, ID_S, ks > 0 ? 1u : 0u);  // V dO^T
+          umma_ss(tmem + reg, dv + off, ddo + off, ID_S, ks > 0 ? 1u : 0u);  // V dO^T
         }
+        umma_commit(smem_u32(&bars->dp_full));
       }
       __syncwarp();
     };
-    auto issue_st = [&](uint32_t slot) {
+    // S^T = K Q_i^T into score region `reg`
+    auto issue_st = [&](uint32_t slot, uint32_t reg) {
       if (elect_one()) {
         const uint64_t dq = dB + ((slot * LY::PAIR_BYTES) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * LY::CHUNK_BYTES + (ks & 3) * 32) >> 4;
-          umma_ss(tmem + T_S, dA + off, dq + off, ID_S, ks > 0 ? 1u : 0u);   // K Q^T
+          umma_ss(tmem + reg, dA + off, dq + off, ID_S, ks > 0 ? 1u : 0u);   // K Q^T
         }
         umma_commit(smem_u32(&bars->s_full));
       }
       __syncwarp();
     };
-    // Per query tile i: P^T and dS^T go back over S^T, so dP^T's columns are free once the
-    // elementwise warps have read them: dP^T(i+1) is issued during their pass over tile i,
-    // S^T(i+1) after dV(i) and dK(i), which read P^T(i) and dS^T(i).
-    uint32_t f_ph = 0;
+    // Per query tile g: P^T and dS^T go back over S^T(g), so S^T(g+1) is computed into the
+    // region of dP^T(g) as soon as the elementwise warps have read dP^T(g), which they do
+    // after storing P^T(g): the next tile's scores are ready when they finish tile g. Then
+    // dV(g) (P^T(g) stored), dK(g) (dS^T(g) stored), and dP^T(g+1) into S^T(g)'s region,
+    // which dK(g) has read (tcgen05 ops of one thread run in issue order).
+    // Under dropout the elementwise warps take S^T and dP^T together, in one pass that
+    // keeps the keep bits live once (a pass split around the dP^T read spills and is
+    // slower): the regions stay fixed (S^T in [0, 128), dP^T in [128, 256)), dP^T(g+1) is
+    // issued once they have read tile g, and S^T(g+1) after dK(g).
     for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, k0, i0, n_q;
       item_tiles(t, bh, k0, i0, n_q);
@@ -667,20 +679,30 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       if (!ok) break;
       a_ph ^= 1;
       tc_fence_after();
-      issue_dpt(i_glob % LY::SLOTS);
-      issue_st(i_glob % LY::SLOTS);
+      if constexpr (DROP) {
+        issue_dpt(i_glob % LY::SLOTS, 128u);
+        issue_st(i_glob % LY::SLOTS, 0u);  // its commit also covers dP^T
+      } else {
+        issue_st(i_glob % LY::SLOTS, (i_glob & 1u) * 128u);
+        issue_dpt(i_glob % LY::SLOTS, ((i_glob & 1u) ^ 1u) * 128u);
+      }
       for (int i = 0; i < n_q; ++i) {
-        const uint32_t slot = (i_glob + i) % LY::SLOTS;
-        const uint32_t nslot = (i_glob + i + 1) % LY::SLOTS;
+        const uint32_t g = i_glob + i;
+        const uint32_t reg_s = DROP ? 0u : (g & 1u) * 128u, reg_dp = reg_s ^ 128u;
+        const uint32_t slot = g % LY::SLOTS;
+        const uint32_t nslot = (g + 1) % LY::SLOTS;
         const bool has_next = i + 1 < n_q;
-        ok = wait_all(smem_u32(&bars->sdp_free), f_ph);
+        ok = wait_all(smem_u32(&bars->dp_read), r_ph);
         if (!ok) break;
-        f_ph ^= 1;
+        r_ph ^= 1;
         if (has_next) {
-          ok = wait_all(smem_u32(&bars->full[nslot]), ((i_glob + i + 1) / LY::SLOTS) & 1u);
+          ok = wait_all(smem_u32(&bars->full[nslot]), ((g + 1) / LY::SLOTS) & 1u);
           if (!ok) break;
           tc_fence_after();
-          issue_dpt(nslot);
+          if constexpr (DROP)
+            issue_dpt(nslot, reg_dp);
+          else
+            issue_st(nslot, reg_dp);
         }
         const uint64_t dq = dBmn + ((slot * LY::PAIR_BYTES) >> 4);
         ok = wait_all(smem_u32(&bars->pt_full), pt_ph);
@@ -691,7 +713,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           const uint64_t ddo = dq + (LY::TILE_BYTES >> 4);
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks) {  // dV += P^T dO_i (K = 128 queries)
-            umma_ts(tmem + T_DV, tmem + T_S + ks * 8, ddo + ((ks * 16 * 128) >> 4), ID_G,
+            umma_ts(tmem + T_DV, tmem + reg_s + ks * 8, ddo + ((ks * 16 * 128) >> 4), ID_G,
                     (i > 0 || ks > 0) ? 1u : 0u);
           }
         }
@@ -703,7 +725,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < BM / 16; ++ks) {  // dK += dS^T Q_i
-            umma_ts(tmem + T_DK, tmem + T_S + 64 + ks * 8, dq + ((ks * 16 * 128) >> 4), ID_G,
+            umma_ts(tmem + T_DK, tmem + reg_s + 64 + ks * 8, dq + ((ks * 16 * 128) >> 4), ID_G,
                     (i > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(smem_u32(&bars->release[slot]));  // Q_i, dO_i: no further reader
@@ -713,7 +735,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           }
         }
         __syncwarp();
-        if (has_next) issue_st(nslot);
+        if (has_next) {
+          if constexpr (DROP)
+            issue_st(nslot, reg_s);
+          else
+            issue_dpt(nslot, reg_s);
+        }
       }
       i_glob += n_q;
     }
@@ -727,18 +754,22 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const int hf = warp >> 2;         // column half: queries [64 hf, 64 hf + 64) of each tile
     const int r = wq * 32 + lane;     // key row of the tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + T_S + hf * 64, tDP = tmem + lane_off + T_DP + hf * 64;
-    // this half's 16-bit P^T at S^T columns [32 hf, 32 hf + 32), dS^T 64 columns further
-    const uint32_t tPT = tmem + lane_off + T_S + hf * 32;
     const uint32_t tK = tmem + lane_off + T_DK, tV = tmem + lane_off + T_DV;
-    uint32_t s_ph = 0, d_ph = 0;
+    uint32_t s_ph = 0, dp_ph = 0, d_ph = 0;
+    uint32_t gq = 0;  // query tiles processed by this CTA (selects the score regions)
     bool ok = true;
     for (int rr_ = 0, t = bw_item_of(0); t < p.n_items && ok; t = bw_item_of(++rr_)) {
       int bh, k0, i0, n_q;
       item_tiles(t, bh, k0, i0, n_q);
       const int key = k0 + r;
-      for (int i = 0; i < n_q; ++i) {
+      for (int i = 0; i < n_q; ++i, ++gq) {
         const int q0 = (i0 + i) * BM;
+        // this half's scores: S^T columns [64 hf, 64 hf + 64) of region gq & 1, dP^T the same
+        // columns of the other region; the 16-bit P^T goes to columns [32 hf, 32 hf + 32) of
+        // S^T's region and dS^T 64 columns further
+        const uint32_t reg_s = DROP ? 0u : (gq & 1u) * 128u, reg_dp = reg_s ^ 128u;
+        const uint32_t tS = tmem + lane_off + reg_s + hf * 64, tDP = tmem + lane_off + reg_dp + hf * 64;
+        const uint32_t tPT = tmem + lane_off + reg_s + hf * 32;
         // dropout: bit (c & 31) of zb[c >> 5] is the keep bit of query
         // q0 + 64 hf + c (c < 64) for this thread's key. Each lane of a 16-key group draws the
         // call of one query row for its group; a shuffle hands the group's 16-bit mask on.
@@ -782,15 +813,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         uint32_t sr[2][32], dr[2][32];
         tmem_ld32(tS, sr[0]);
         tmem_ld32(tS + 32, sr[1]);
-        tmem_ld32(tDP, dr[0]);
-        tmem_ld32(tDP + 32, dr[1]);
+        if constexpr (DROP) {  // dP^T is ready with S^T (see the MMA warp)
+          tmem_ld32(tDP, dr[0]);
+          tmem_ld32(tDP + 32, dr[1]);
+        }
         tmem_wait_ld();
-        reg_fence(sr[0]); reg_fence(sr[1]); reg_fence(dr[0]); reg_fence(dr[1]);
-        // both halves hold their scores in registers: S^T may now take P^T and dS^T, and
-        // dP^T's columns the next tile's product
+        reg_fence(sr[0]); reg_fence(sr[1]);
+        if constexpr (DROP) {
+          reg_fence(dr[0]); reg_fence(dr[1]);
+        }
+        // both halves hold their scores in registers: S^T's columns may now take P^T, dS^T
         tc_fence_before();
         named_bar_sync(3, BW_EW_WARPS * 32);
-        if (lane == 0) mbar_arrive(smem_u32(&bars->sdp_free));
+        if constexpr (DROP) {
+          if (lane == 0) mbar_arrive(smem_u32(&bars->dp_read));
+        }
         // in phases over all 64 values (exponent arguments, exponentials, products), so
         // that the exponentials issue back to back instead of one dependent chain per pair
         const uint64_t c2 = f2(p.c, p.c);
@@ -815,8 +852,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                 hf * 64 + e >= qfirst ? ex2_approx(__uint_as_float(sr[e >> 5][e & 31])) : 0.f);
         }
         if constexpr (!DROP) {
-          // P^T first, signalled on its own: the dV product needs nothing else and runs
-          // while dS^T = P^T o (dP^T - D) is computed and stored
+          // P^T first
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pp[16];
@@ -829,6 +865,21 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->pt_full));
+          // then dP^T: the same outcome in every elementwise warp (a timeout ends the loop
+          // everywhere, never at a barrier); once read, its region may take S^T(g+1)
+          ok = named_bar_red_and(4, BW_EW_WARPS * 32,
+                                 wait_bar(smem_u32(&bars->dp_full), dp_ph, abort_flag, lim));
+          if (!ok) break;
+          dp_ph ^= 1;
+          tc_fence_after();
+          tmem_ld32(tDP, dr[0]);
+          tmem_ld32(tDP + 32, dr[1]);
+          tmem_wait_ld();
+          reg_fence(dr[0]); reg_fence(dr[1]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->dp_read));
+          // dS^T = P^T o (dP^T - D)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pd[16];
@@ -844,9 +895,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
             tmem_st16(tPT + 64 + c * 16, pd);
           }
         } else {
-          // under dropout one pass builds both operands (P^T o Z and dS^T = P^T o (dP^T o Z - D),
-          // Z's 1/(1-p) applied to dV at the end): a split pass spills the keep bits and is
-          // slower than the overlap it buys
+          // one pass builds both operands: P^T o Z and dS^T = P^T o (dP^T o Z - D) (Z's
+          // 1/(1-p) is applied to dV at the end)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pp[16], pd[16];
