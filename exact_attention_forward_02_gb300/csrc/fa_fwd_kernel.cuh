@@ -580,7 +580,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t stg = sStage + g * STAGE_BYTES;
     // Merge of every piece of (item, Q tile g) from the workspace, four rows per lane. The
     // arithmetic and its order are those of the softmax warps' merge, so the result does
-    // not depend on which piece completes the count.
+    // not depend on which piece completes the count: l is summed with explicit
+    // non-contracted products and sums (an FMA contraction chosen differently in two
+    // places would round differently), O~ with explicit fmaf.
     auto merge_from_workspace = [&](int item, int bh, int q0) {
       const long long W = (long long)p.n_items * p.n_kv_all;
       const long long G = gridDim.x;
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const float m1 = __ldcg(p1 + D * BM), l1 = __ldcg(p1 + (D + 1) * BM);
           m = fmaxf(m0, m1);
           const float w0 = ex2_approx(m0 - m), w1 = ex2_approx(m1 - m);
-          l = l0 * w0 + l1 * w1;
+          l = __fadd_rn(__fmul_rn(l0, w0), __fmul_rn(l1, w1));
           const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
           const float a0 = w0 * inv_l, a1 = w1 * inv_l;
 #pragma unroll 1
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           l = 0.f;
           for (int cc = c0; cc <= c1; ++cc) {
             const float* pc = piece(cc);
-            l += __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
+            l = __fadd_rn(l, __fmul_rn(__ldcg(pc + (D + 1) * BM), ex2_approx(__ldcg(pc + D * BM) - m)));
           }
           const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
 #pragma unroll 1
@@ -1010,7 +1012,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int k = 0; k < 32; ++k) x[hh][k] = __ldcg(po + (hh * 32 + k) * BM);
               m = fmaxf(m_run, mo);
               const float w_own = ex2_approx(m_run - m), w_o = ex2_approx(mo - m);
-              l = first ? l_run * w_own + lo * w_o : lo * w_o + l_run * w_own;
+              l = first ? __fadd_rn(__fmul_rn(l_run, w_own), __fmul_rn(lo, w_o))
+                        : __fadd_rn(__fmul_rn(lo, w_o), __fmul_rn(l_run, w_own));
               const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
               const float a_own = w_own * inv_l, a_o = w_o * inv_l;
               const float a0 = first ? a_own : a_o, a1 = first ? a_o : a_own;
@@ -1054,8 +1057,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               l = 0.f;
               for (int cc = c0; cc <= c1; ++cc) {
                 const float* pc = piece(cc);
-                l += cc == me ? l_run * ex2_approx(m_run - m)
-                              : __ldcg(pc + (D + 1) * BM) * ex2_approx(__ldcg(pc + D * BM) - m);
+                const float lc = cc == me ? l_run : __ldcg(pc + (D + 1) * BM);
+                const float mc = cc == me ? m_run : __ldcg(pc + D * BM);
+                l = __fadd_rn(l, __fmul_rn(lc, ex2_approx(mc - m)));
               }
               const float inv_l = (l > 0.f ? 1.f / l : 0.f) * oscale;
               const float a_own = ex2_approx(m_run - m) * inv_l;
