@@ -574,7 +574,7 @@ def _oracle_sample(budget_s: float, seed: int = 0):
         qh, kh, vh = _oracle_head(name)
         n_rows = 0
         spent = 0.0
-        batch = max(threads * 4, 64)
+        batch = max(threads * 32, 256)  # enough rows per call to keep every thread busy
         while spent < share:
             rows = rng.integers(0, w.Nq, size=batch)
             t0 = time.perf_counter()
@@ -603,7 +603,9 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # host seconds of oracle work per step: the whole --steps/--warmup run stays near 100 s
+    # of oracle time (each step still times at least one batch of rows of each workload)
+    per_step = min(10.0, 100.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         _oracle_sample(per_step, seed=1)
     vals, secs = [], 0.0
@@ -624,7 +626,7 @@ def run_reference(args):
         "config": {"workload": "+".join(WORKLOADS),
                    "note": "float64 CPU oracle on bounded row samples per step"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"per step: {desc}; about {per_step:.1f} s of host time"},
+                         "sample": f"per step: {desc}; about {per_step:.3g} s of host time"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
