@@ -591,10 +591,58 @@ def _oracle_sample(budget_s: float, seed: int = 0):
     return total_flops / total_s / 1e12, total_s, threads, "; ".join(desc)
 
 
+def _oracle_single_core(budget_s: float = 2.0):
+    """The oracle on one thread: the two 128 x 128 d=64 workloads whole (full and causal),
+    and random rows of the d=64 cross-attention workload for about budget_s seconds."""
+    import numpy as np
+
+    import gen
+    import oracle
+
+    out = {}
+    for name in ("tiny", "tiny_causal"):
+        w = gen.WORKLOADS[name]
+        q, k, v = (gen.to_f64_numpy(t) for t in gen.make_qkv(w))
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.attention(q, k, v, w.scale, w.causal, nthreads=1)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 0.2:
+                break
+        out[name] = round(w.flops * reps / dt / 1e12, 6)
+    w = gen.WORKLOADS["b4h12_q1000_k4097_d64_cross"]
+    heads = tuple(gen.to_f64_numpy(t[:1, :1]) for t in gen.make_qkv(w))  # head (0, 0)
+    rng = np.random.default_rng(7)
+    n_rows, spent = 0, 0.0
+    while spent < budget_s:
+        rows = rng.integers(0, w.Nq, size=64)
+        t0 = time.perf_counter()
+        oracle.attention_rows(*heads, w.scale, w.causal, rows, nthreads=1)
+        spent += time.perf_counter() - t0
+        n_rows += rows.size
+    out[w.name] = round(4.0 * w.Nk * w.d * n_rows / spent / 1e12, 6)
+    out["sample"] = (f"one thread; tiny and tiny_causal whole; {n_rows} random rows of head (0,0) "
+                     f"of {w.name}, {spent:.1f} s")
+    return out
+
+
 def cpu_baseline(budget_s: float):
     tf, secs, threads, desc = _oracle_sample(budget_s)
-    return {"value": round(tf, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+    line = {"value": round(tf, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{desc}; float64, {secs:.1f} s of host time; FLOPs 4*visible_keys*d per row"}
+    try:
+        line["single_core"] = _oracle_single_core()
+    except Exception as e:  # reported, never allowed to suppress the bench line
+        line["single_core"] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
+    return line
+
+
+def reference_step_budget(steps: int, warmup: int) -> float:
+    """Host seconds of oracle work per reference-arm step: the whole --steps/--warmup run
+    holds about 100 s of oracle time, 10 s per step at most (each step still times at
+    least one batch of rows of each workload, so a step never does zero work)."""
+    return min(10.0, 100.0 / max(1, steps + warmup))
 
 
 def run_reference(args):
@@ -603,9 +651,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    # host seconds of oracle work per step: the whole --steps/--warmup run stays near 100 s
-    # of oracle time (each step still times at least one batch of rows of each workload)
-    per_step = min(10.0, 100.0 / max(1, args.steps + args.warmup))
+    per_step = reference_step_budget(args.steps, args.warmup)
     for _ in range(args.warmup):
         _oracle_sample(per_step, seed=1)
     vals, secs = [], 0.0
