@@ -411,8 +411,10 @@ def secondary_measurements(args):
     """The library's other paths, each timed by this script in its own process the same way
     (L2 flushed before every launch, CUDA events on the launching stream, medians over the
     steps): the backward pass, dropout forward and backward, E4M3 inputs, plain fa_fwd (no
-    stream-K) on the full N=4096 workload, and the d=64 cross-attention shape with and
-    without stream-K. Not part of the headline metric."""
+    stream-K) on the full N=4096 workload, the d=64 cross-attention shape with and without
+    stream-K, the B=1, H=16, N=32768 causal workload and the two 128 x 128 d=64 workloads,
+    so that every workload of the method's test set has a measured rate. Not part of the
+    headline metric."""
     runs = {
         "bwd": ["--bwd"],
         "bwd_dropout_0.1": ["--bwd", "--dropout", "0.1"],
@@ -421,6 +423,8 @@ def secondary_measurements(args):
         "fwd_full_n4096_plain_fa_fwd": ["--workloads", "b2h8_n4096_d128_full", "--sched", "plain"],
         "fwd_cross_d64_plain": ["--workloads", "b4h12_q1000_k4097_d64_cross", "--sched", "plain"],
         "fwd_cross_d64_streamk": ["--workloads", "b4h12_q1000_k4097_d64_cross", "--sched", "auto"],
+        "fwd_n32768_causal_x2": ["--workloads", "b1h16_n32768_d128_causal_x2"],
+        "fwd_tiny_full_and_causal": ["--workloads", "tiny,tiny_causal"],
     }
     steps = str(max(20, min(args.steps, 100)))
     out = {}
@@ -432,7 +436,8 @@ def secondary_measurements(args):
             line = json.loads(r.stdout.strip().splitlines()[-1])
             out[name] = {"value": line["value"], "unit": line["unit"],
                          "entry_point": line["config"].get("entry_point"),
-                         "breakdown": {k: {"ms": v["ms"], "tflops": v["tflops"]}
+                         "breakdown": {k: {"ms": v["ms"], "tflops": v["tflops"],
+                                           "pct_of_peak": v.get("pct_of_peak")}
                                        for k, v in line.get("breakdown", {}).items()}}
         except Exception as e:  # a failed side run is reported, never hidden
             out[name] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
