@@ -23,3 +23,32 @@ def test_single_core_oracle_figures(oracle_mod):
     for name in ("tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross"):
         assert out[name] > 0, out
     assert "one thread" in out["sample"]
+
+
+def test_failed_side_run_is_reported_not_raised(monkeypatch):
+    import subprocess
+    import types
+
+    calls = []
+
+    def fake_run(cmd, **kw):
+        calls.append(cmd)
+        if "--bwd" in cmd:
+            raise subprocess.TimeoutExpired(cmd, 600)
+        if "--fp8" in cmd:
+            return types.SimpleNamespace(stdout="", stderr="boom", returncode=1)
+        line = ('{"value": 1.5, "unit": "TFLOPS", "config": {"entry_point": "fa_fwd"}, '
+                '"breakdown": {"w": {"ms": 0.1, "tflops": 1.5, "pct_of_peak": 0.1}}}')
+        return types.SimpleNamespace(stdout="noise\n" + line + "\n", stderr="", returncode=0)
+
+    monkeypatch.setattr(subprocess, "run", fake_run)
+    args = types.SimpleNamespace(steps=2000)
+    out = bench.secondary_measurements(args)
+    assert len(calls) == len(out)
+    assert "error" in out["bwd"] and "TimeoutExpired" in out["bwd"]["error"]
+    assert "error" in out["fwd_fp8_e4m3"]
+    ok = out["fwd_tiny_full_and_causal"]
+    assert ok["value"] == 1.5 and ok["breakdown"]["w"]["pct_of_peak"] == 0.1
+    for cmd in calls:  # every side run is a bounded, single-purpose bench process
+        assert "--no-also" in cmd and "--cpu-budget" in cmd
+        assert cmd[cmd.index("--steps") + 1] == "100"
