@@ -213,18 +213,32 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     """
     import torch
 
+    # Every check runs before anything touches a device: the kernels write through raw
+    # pointers, so a caller-supplied `out`, `lse` or `workspace` of the wrong size, type,
+    # layout or device would be written out of bounds.
     if q.dtype not in (torch.float16, torch.bfloat16):
         raise TypeError("q, k, v must be float16 or bfloat16")
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share one dtype")
-    if not (q.is_cuda and k.is_cuda and v.is_cuda):
-        raise ValueError("q, k, v must be CUDA tensors")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("expected [B, H, N, d] tensors")
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
         raise ValueError("k and v must be [B, H, Nk, d] with q's B, H, d")
+    if out is not None and (out.dtype != q.dtype or tuple(out.shape) != (B, H, Nq, d)
+                            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous [B, H, Nq, d] tensor of q's dtype")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous [B, H, Nq] float32 tensor")
+    if workspace is not None and (workspace.dtype != torch.uint8 or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous uint8 tensor")
+    tensors = [t for t in (q, k, v, out, lse, workspace) if t is not None]
+    if not all(t.is_cuda for t in tensors):
+        raise ValueError("q, k, v (and out, lse, workspace when given) must be CUDA tensors")
+    if any(t.device != q.device for t in tensors):
+        raise ValueError("q, k, v (and out, lse, workspace when given) must be on one device")
     q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     if out is None:
         out = torch.empty_like(q)
