@@ -360,6 +360,7 @@ def run_ours(args):
             ms = statistics.fmean(per[w.name])
             breakdown[w.name] = {"ms": round(ms, 5), "tflops": round(w.flops / (ms * 1e-3) / 1e12, 1),
                                  "pct_of_peak": round(100 * w.flops / (ms * 1e-3) / 1e12 / peak, 1),
+                                 "ms_median": round(statistics.median(per[w.name]), 5),
                                  "ms_min": round(min(per[w.name]), 5), "ms_max": round(max(per[w.name]), 5)}
         cpu = cpu_baseline(budget_s=args.cpu_budget) if (args.cpu_budget > 0 and ws == 1) else None
         also = secondary_measurements(args) if (ws == 1 and args.also and not (
