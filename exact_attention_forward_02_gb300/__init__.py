@@ -26,7 +26,11 @@ STATUS = {
     -4: "FA_ERR_EMPTY_KEYS", -5: "FA_ERR_SCALE", -6: "FA_ERR_ALIGN", -7: "FA_ERR_DTYPE",
     -8: "FA_ERR_CUDA", -9: "FA_ERR_TENSOR_MAP", -10: "FA_ERR_DEVICE", -11: "FA_ERR_TIMEOUT",
     -12: "FA_ERR_WORKSPACE", -13: "FA_ERR_SCRATCH_LIMIT", -14: "FA_ERR_DROPOUT",
+    -15: "FA_ERR_RANGE",
 }
+FA_WAIT_LIMIT_DEFAULT_US = 2_000_000
+FA_WAIT_LIMIT_MIN_US = 100
+FA_WAIT_LIMIT_MAX_US = 3_600_000_000
 FA_NOALLOC_SCRATCH_BYTES = 48 << 20
 globals().update({v: k for k, v in STATUS.items()})
 
@@ -91,6 +95,10 @@ def _load() -> ctypes.CDLL:
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
     lib.fa_num_kernel_launches.restype = ctypes.c_longlong
     lib.fa_num_kernel_launches.argtypes = []
+    lib.fa_set_wait_limit_us.restype = ctypes.c_int
+    lib.fa_set_wait_limit_us.argtypes = [ctypes.c_ulonglong]
+    lib.fa_get_wait_limit_us.restype = ctypes.c_ulonglong
+    lib.fa_get_wait_limit_us.argtypes = []
     return lib
 
 
@@ -200,6 +208,16 @@ def fa_selftest_wait_timeout(limit_us: int, stream=None) -> int:
 
 def fa_num_kernel_launches() -> int:
     return int(lib.fa_num_kernel_launches())
+
+
+def fa_set_wait_limit_us(limit_us: int) -> int:
+    if not 0 <= int(limit_us) < 1 << 64:
+        return FA_ERR_RANGE
+    return int(lib.fa_set_wait_limit_us(int(limit_us)))
+
+
+def fa_get_wait_limit_us() -> int:
+    return int(lib.fa_get_wait_limit_us())
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

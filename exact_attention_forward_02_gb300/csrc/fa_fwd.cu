@@ -24,8 +24,11 @@ namespace {
 
 using namespace fa;
 
-constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait
+// Time limit of every device-side pipeline wait, read when a kernel is launched
+// (fa_set_wait_limit_us); 2 s unless the caller changes it.
+std::atomic<unsigned long long> g_wait_limit_ns{FA_WAIT_LIMIT_DEFAULT_US * 1000ull};
 std::atomic<long long> g_launches{0};
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -152,7 +155,8 @@ WsPlan ws_plan(long long BH, int Nq, int Nk, int d, int sms) {
   w.W = w.n_items * w.n_kv;
   w.G = (int)(w.W < sms ? w.W : sms);
   auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  w.part_bytes = align((size_t)w.G * 2 * 2 * BM * (d + 4) * sizeof(float));
+  // [CTA][slot 2][Q tile 2][part_cols(d)][128 rows] fp32, as the kernel indexes it
+  w.part_bytes = align((size_t)w.G * 2 * 2 * BM * part_cols(d) * sizeof(float));
   w.cnt_bytes = align((size_t)w.n_items * 2 * sizeof(int));
   w.total = w.part_bytes + w.cnt_bytes;
   return w;
@@ -237,7 +241,7 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   p.n_items = (int)(p.n_qblk * BH);
   p.n_kv_all = (Nk + BN - 1) / BN;
   p.c = scale * 1.4426950408889634f;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.wait_limit_ns = wait_limit_ns();
   p.streamk = 0;
   p.ws_part = nullptr;
   p.ws_cnt = nullptr;
@@ -374,7 +378,7 @@ int run_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int 
   p.n_items = (int)(p.n_qblk * BH);
   p.n_kv_all = (Nk + BN - 1) / BN;
   p.c = (float)c;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.wait_limit_ns = wait_limit_ns();
   p.streamk = 0;
   p.ws_part = nullptr;
   p.ws_cnt = nullptr;
@@ -769,7 +773,7 @@ static int run_bwd(const void* Q, const void* K, const void* V, const void* O, c
   p.n_items = 0;
   p.c = scale * 1.4426950408889634f;
   p.scale = scale;
-  p.wait_limit_ns = kDefaultWaitLimitNs;
+  p.wait_limit_ns = wait_limit_ns();
   p.drop_bias = 0;
   p.drop_offset = 0;
   p.drop_rscale = 1.f;
@@ -841,6 +845,7 @@ const char* fa_strerror(int code) {
       return "the problem needs more scratch than fa_fwd_noalloc's fixed array (FA_NOALLOC_SCRATCH_BYTES)";
     case FA_ERR_DROPOUT:
       return "dropout probability must be finite, >= 0 and below 1 - 2^-9";
+    case FA_ERR_RANGE: return "argument outside its documented range";
     default: return "unknown status code";
   }
 }
@@ -857,5 +862,13 @@ int fa_selftest_wait_timeout(int limit_us, void* stream) {
 }
 
 long long fa_num_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int fa_set_wait_limit_us(unsigned long long limit_us) {
+  if (limit_us < FA_WAIT_LIMIT_MIN_US || limit_us > FA_WAIT_LIMIT_MAX_US) return FA_ERR_RANGE;
+  g_wait_limit_ns.store(limit_us * 1000ull, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+unsigned long long fa_get_wait_limit_us(void) { return wait_limit_ns() / 1000ull; }
 
 }  // extern "C"

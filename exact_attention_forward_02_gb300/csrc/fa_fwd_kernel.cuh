@@ -62,6 +62,9 @@ constexpr uint32_t TMEM_COLS = 512;      // S0 | S1 | O0 | O1, 128 columns each
 constexpr uint32_t TMEM_S0 = 0, TMEM_O0 = 256;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O~ only when m grows > 2^8
 constexpr int SMEM_LIMIT = 232448;       // 227 KB opt-in dynamic shared memory per CTA
+// Columns of one stream-K partial state (O~[d], m, l), each stored for the 128 rows of a
+// Q tile; the host sizes the workspace with the same function.
+__host__ __device__ constexpr int part_cols(int d) { return d + 2; }
 constexpr int MAX_SLOTS = 8;
 // Epilogue stage of one Q tile: one 64-column box of O in 16 bits (128 rows x 128 bytes,
 // 128-byte swizzled as the O tensor map expects) or 32 fp32 columns of a partial state.
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   static_assert(!(FP8 && DROP), "dropout is not combined with E4M3 inputs");
   static_assert(!FP8 || D == 128, "E4M3 inputs need d = 128 (one 128-byte row per tile row)");
   using LY = Layout<D, FP8 ? 1 : 2>;
-  constexpr int PART_COLS = D + 2;  // O~[D], m, l of a row, each column stored for 128 rows
+  constexpr int PART_COLS = part_cols(D);  // O~[D], m, l of a row, each stored for 128 rows
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);

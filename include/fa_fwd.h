@@ -43,8 +43,15 @@ enum {
   FA_ERR_TIMEOUT = -11,    /* device-side: a pipeline wait exceeded its time limit        */
   FA_ERR_WORKSPACE = -12,  /* fa_fwd_ws: workspace missing or too small                   */
   FA_ERR_SCRATCH_LIMIT = -13, /* fa_fwd_noalloc: needs more than FA_NOALLOC_SCRATCH_BYTES  */
-  FA_ERR_DROPOUT = -14     /* dropout probability negative, not finite or too close to 1  */
+  FA_ERR_DROPOUT = -14,    /* dropout probability negative, not finite or too close to 1  */
+  FA_ERR_RANGE = -15       /* an argument outside its documented range                    */
 };
+
+/* Limits of fa_set_wait_limit_us, in microseconds: the default (2 s), the smallest and the
+ * largest accepted value (100 us and one hour). */
+#define FA_WAIT_LIMIT_DEFAULT_US 2000000ull
+#define FA_WAIT_LIMIT_MIN_US 100ull
+#define FA_WAIT_LIMIT_MAX_US 3600000000ull
 
 /* Size of the fixed device scratch array behind fa_fwd_noalloc (48 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES (48u << 20)
@@ -63,7 +70,9 @@ enum {
  *   stream a cudaStream_t (NULL = the legacy default stream)
  *
  * Layout: no padding; row i of head (b, h) of Q starts at element ((b*H + h)*Nq + i)*d.
- * Ownership: the library allocates no device memory and keeps no pointer after return.
+ * Ownership: calls allocate no device memory and keep no pointer after return. (Every
+ *   device that loads the library does hold one fixed array of FA_NOALLOC_SCRATCH_BYTES,
+ *   the scratch of fa_fwd_noalloc, until the process exits; fa_fwd never touches it.)
  * Timing: asynchronous. Returns FA_OK once the launch is queued; O and L are valid
  *   after `stream` is synchronised. Calls on different streams that write the same
  *   O/L race.
@@ -270,6 +279,21 @@ const char* fa_strerror(int code);
  * usable. Returns FA_OK once queued, FA_ERR_SHAPE for a limit out of range, FA_ERR_DEVICE
  * or FA_ERR_CUDA on failure to launch. */
 int fa_selftest_wait_timeout(int limit_us, void* stream);
+
+/* fa_set_wait_limit_us -- time limit of every device-side pipeline wait (an mbarrier wait
+ * of a kernel role on another role: a TMA copy landing, a tensor-core product completing,
+ * a softmax warp handing P over) for the kernels launched after this call, process-wide and
+ * on every device. A wait that exceeds it gives up: the kernel records FA_ERR_TIMEOUT (read
+ * with fa_last_status), stops every role of its CTA, drains its in-flight copies and
+ * products, frees its Tensor Memory and returns; O, L (or the gradients) are then undefined.
+ * The default, FA_WAIT_LIMIT_DEFAULT_US (2 s), is hundreds of times the longest legitimate
+ * wait of an unshared GPU; callers whose GPU is time-sliced or preempted by other work
+ * (where a CTA can be descheduled for longer) raise it. No CUDA call is made.
+ *   limit_us  FA_WAIT_LIMIT_MIN_US .. FA_WAIT_LIMIT_MAX_US; anything else returns
+ *             FA_ERR_RANGE and leaves the limit unchanged.
+ * fa_get_wait_limit_us -- the current limit in microseconds. */
+int fa_set_wait_limit_us(unsigned long long limit_us);
+unsigned long long fa_get_wait_limit_us(void);
 
 /* fa_num_kernel_launches -- number of kernels libfa has launched in this process
  * (all devices), for accounting launches in a timed region. */

@@ -81,6 +81,23 @@ def test_selftest_rejects_out_of_range_limit():
     assert fa.fa_selftest_wait_timeout(2_000_000) == fa.FA_ERR_SHAPE
 
 
+def test_wait_limit_setter_checks_its_range_and_makes_no_cuda_call():
+    """fa_set_wait_limit_us accepts FA_WAIT_LIMIT_MIN_US..FA_WAIT_LIMIT_MAX_US, rejects the
+    rest with FA_ERR_RANGE and then keeps the previous limit; it touches no device."""
+    import exact_attention_forward_02_gb300 as fa
+    assert fa.fa_get_wait_limit_us() == fa.FA_WAIT_LIMIT_DEFAULT_US == 2_000_000
+    try:
+        for bad in (0, 99, fa.FA_WAIT_LIMIT_MAX_US + 1, 1 << 63, -1):
+            assert fa.fa_set_wait_limit_us(bad) == fa.FA_ERR_RANGE, bad
+            assert fa.fa_get_wait_limit_us() == fa.FA_WAIT_LIMIT_DEFAULT_US
+        for good in (fa.FA_WAIT_LIMIT_MIN_US, 5_000_000, fa.FA_WAIT_LIMIT_MAX_US):
+            assert fa.fa_set_wait_limit_us(good) == fa.FA_OK
+            assert fa.fa_get_wait_limit_us() == good
+    finally:
+        assert fa.fa_set_wait_limit_us(fa.FA_WAIT_LIMIT_DEFAULT_US) == fa.FA_OK
+    assert "range" in fa.strerror(fa.FA_ERR_RANGE)
+
+
 def test_workspace_variant_host_checks():
     """fa_fwd_ws shares fa_fwd's host-side checks; sizes are 0 for invalid or causal calls."""
     import exact_attention_forward_02_gb300 as fa

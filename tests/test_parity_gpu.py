@@ -1,9 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle, element by
 element, on the same seeded inputs.
 
-Small and medium cases are compared on every output element; the full-size workloads
-(in the launch configuration the benchmark times) are compared on sampled rows that the
-oracle computes one by one, plus properties that hold at any size.
+Every case, the full-size workloads included, is compared on every output element, plus
+properties that hold at any size (causal row 0).
 """
 import ctypes
 
@@ -12,7 +11,7 @@ import pytest
 import torch
 
 import gen
-from tests.fa_testlib import TOL_L, TOL_O, compare, oracle_rows, run_cuda, sample_rows
+from tests.fa_testlib import TOL_L, TOL_O, compare, oracle_whole, p_rounding_term, run_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +81,7 @@ def test_small_full_compare(case):
         assert r["raw_ok"], r
 
 
-@pytest.mark.parametrize("name", ["tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross"])
+@pytest.mark.parametrize("name", ["tiny", "tiny_causal"])
 def test_workload_full_compare(name):
     w = gen.WORKLOADS[name]
     r = _full_case(w)
@@ -92,18 +91,24 @@ def test_workload_full_compare(name):
 
 @pytest.mark.parametrize("name", ["b2h8_n4096_d128_full", "b2h8_n8192_d128_causal",
                                   "b1h16_n32768_d128_causal_x2", "b4h12_q1000_k4097_d64_cross"])
-def test_workload_sampled_rows(name):
-    """Full-size workloads, launched exactly as the benchmark launches them, checked on
-    sampled rows (head boundaries, tile edges, random rows) against the oracle."""
+def test_workload_whole_output(name):
+    """Full-size workloads through fa_fwd (the entry point without a workspace; the
+    benchmark's fa_fwd_ws launches of the two full-attention workloads are checked the same
+    way in test_streamk_gpu.py): every element of O and L against the oracle's whole
+    output."""
     w = gen.WORKLOADS[name]
-    q, k, v = gen.make_qkv(w)
+    (q, k, v), (Oref, Lref) = oracle_whole(name)
     O, L = run_cuda(w, q, k, v)
-    rows = sample_rows(w)
-    Oref, Lref = oracle_rows(w, q, k, v, rows)
-    r = compare(w, O, L, Oref, Lref, rows=rows)
-    print(name, r)
-    assert r["graded_ok"], r
-    if name != "b1h16_n32768_d128_causal_x2":
+    if name == "b1h16_n32768_d128_causal_x2":
+        # V of std 2 (|V| up to ~10): the bf16 rounding of P (2^-9) moves some hundreds of
+        # the 67 M outputs past 1e-2 + half an ulp; graded by the bound derived from that
+        # rounding (p_rounding_term)
+        r = compare(w, O, L, Oref, Lref, extra=p_rounding_term(w, v))
+        print(name, r)
+        assert r["derived_ok"], r
+    else:
+        r = compare(w, O, L, Oref, Lref)
+        print(name, r)
         assert r["raw_ok"], r
     # every row written and finite (NaN canary fill before the call)
     assert torch.isfinite(O).all() and torch.isfinite(L).all()
@@ -176,3 +181,19 @@ def test_bounded_wait_times_out_cleanly_and_context_survives():
     assert fa.fa_last_status() == 0
     r = _full_case(gen.WORKLOADS["tiny_causal"])
     assert r["raw_ok"], r
+
+
+def test_wait_limit_applies_to_later_launches():
+    """A raised library-wide wait limit is taken by the next launches (the forward pass
+    completes with status 0 under it); the self test still times out at its own limit."""
+    import exact_attention_forward_02_gb300 as fa
+    try:
+        assert fa.fa_set_wait_limit_us(30_000_000) == fa.FA_OK
+        r = _full_case(gen.WORKLOADS["tiny"])
+        assert r["raw_ok"], r
+        assert fa.fa_clear_status() == 0
+        assert fa.fa_selftest_wait_timeout(1000) == 0
+        assert fa.fa_last_status() == fa.FA_ERR_TIMEOUT
+        assert fa.fa_clear_status() == 0
+    finally:
+        assert fa.fa_set_wait_limit_us(fa.FA_WAIT_LIMIT_DEFAULT_US) == fa.FA_OK

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import gen
-from tests.fa_testlib import compare, oracle_rows, sample_rows
+from tests.fa_testlib import compare, oracle_whole, run_cuda_ws
 
 pytestmark = pytest.mark.gpu
 
@@ -75,17 +75,20 @@ def test_streamk_full_compare_and_reuse(case):
         assert torch.equal(L, outs[0][1])
 
 
-def test_streamk_full_size_sampled_rows():
-    w = gen.WORKLOADS["b2h8_n4096_d128_full"]
-    q, k, v = gen.make_qkv(w)
-    outs, nbytes = run_ws(w, q, k, v, calls=2)
+@pytest.mark.parametrize("name", ["b2h8_n4096_d128_full", "b4h12_q1000_k4097_d64_cross"])
+def test_streamk_full_size_whole_output(name):
+    """The two full-attention workloads at full size, launched as the benchmark launches
+    them (fa_fwd_ws, two calls on one workspace): every element against the oracle."""
+    w = gen.WORKLOADS[name]
+    (q, k, v), (Oref, Lref) = oracle_whole(name)
+    outs, nbytes = run_cuda_ws(w, q, k, v, calls=2)
     assert nbytes > 0
-    rows = sample_rows(w)
-    Oref, Lref = oracle_rows(w, q, k, v, rows)
     for O, L in outs:
-        r = compare(w, O, L, Oref, Lref, rows=rows)
+        r = compare(w, O, L, Oref, Lref)
         print(w.name, r)
         assert r["raw_ok"], r
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
 
 
 def test_streamk_agrees_with_plain_path():
@@ -122,3 +125,21 @@ def test_workspace_errors_and_causal_ignores_it():
     wc = gen.custom(1, 1, 128, 4096, 128, gen.BF16, True, 1.0, seed=3)
     O2, L2 = run_cuda(wc, *gen.make_qkv(wc))
     assert torch.equal(O.cpu().view(torch.int16), O2.view(torch.int16))
+
+
+@pytest.mark.parametrize("shape", [(2, 8, 4096, 4096, 128), (4, 12, 1000, 4097, 64), (1, 1, 128, 8192, 128)])
+def test_workspace_size_is_the_documented_layout(shape):
+    """fa_fwd_workspace_bytes = the partial states [CTA][slot 2][Q tile 2][d + 2][128 rows]
+    fp32 (O~, m and l) and one int counter per (work item, Q tile), each part rounded up to 256 bytes,
+    with one CTA per SM (or per K/V tile when there are fewer)."""
+    import exact_attention_forward_02_gb300 as fa
+    B, H, Nq, Nk, d = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_items = -(-Nq // 256) * B * H
+    n_kv = -(-Nk // 128)
+    G = min(n_items * n_kv, sms)
+    up = lambda x: -(-x // 256) * 256  # noqa: E731
+    expect = up(G * 2 * 2 * (d + 2) * 128 * 4) + up(n_items * 2 * 4)
+    if n_items % sms == 0:
+        expect = 0
+    assert fa.fa_fwd_workspace_bytes(B, H, Nq, Nk, d, False) == expect
