@@ -65,6 +65,33 @@ def whole_job_tflops(flops_per_rank_step: float, world: int, step_ms_max: float)
     return world * flops_per_rank_step / (step_ms_max * 1e-3) / 1e12
 
 
+EX2_PER_CLK_PER_SM = 32  # ex2.approx rate measured on the GB300 (lanes per clock per SM)
+
+
+def visible_scores(w) -> int:
+    """Scores that take an exponential: one per (row, visible key); causal rows see keys
+    j <= i (top-left), so row i has min(i + 1, Nk) of them."""
+    if not w.causal:
+        return w.B * w.H * w.Nq * w.Nk
+    n = min(w.Nq, w.Nk)
+    per_head = n * (n + 1) // 2 + (w.Nq - n) * w.Nk
+    return w.B * w.H * per_head
+
+
+def sfu_bound(w, ms: float, sms: int, sm_mhz: float) -> dict:
+    """The secondary bound of the forward pass: its exponentials. One ex2 per visible score
+    runs on the special-function pipe, whose measured rate is 32 lanes per clock per SM; the
+    16-bit pack of P (one cvt per two scores) issues to the same pipe, so the pipe carries
+    1.5 lane operations per score."""
+    n = visible_scores(w)
+    peak = EX2_PER_CLK_PER_SM * sms * sm_mhz * 1e6
+    achieved = n / (ms * 1e-3)
+    return {"bound": "sfu", "ex2_count": n, "achieved_ex2_per_s": achieved, "peak_ex2_per_s": peak,
+            "frac": round(achieved / peak, 4), "pipe_frac_with_pack": round(1.5 * achieved / peak, 4),
+            "peak_source": f"{EX2_PER_CLK_PER_SM} ex2/clk/SM x {sms} SMs x {sm_mhz:g} MHz (median SM clock "
+                           "sampled in the timed region)"}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -354,6 +381,8 @@ def run_ours(args):
         dom_ms = statistics.fmean(per[dominant])
         achieved = wd.flops / (dom_ms * 1e-3) / 1e12
         clk = clocks.summary() if clocks else None
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        sm_mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz") or 2070.0
         value = whole_job_tflops(flops_step, ws, step_ms_max)
         breakdown = {}
         for w in wl:
@@ -391,7 +420,8 @@ def run_ours(args):
                          "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} dense (burst: kernel timed alone)",
                          "traffic": recorded_traffic(dominant) if args.dropout == 0 else None,
-                         "algorithmic_bytes": wd.io_bytes},
+                         "algorithmic_bytes": wd.io_bytes,
+                         "secondary": sfu_bound(wd, dom_ms, sms, sm_mhz)},
             "clocks": clk,
             "e2e": {"value": round(whole_job_tflops(flops_step, ws, e2e_ms_max), 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ne2e,
@@ -437,6 +467,7 @@ def secondary_measurements(args):
             line = json.loads(r.stdout.strip().splitlines()[-1])
             out[name] = {"value": line["value"], "unit": line["unit"],
                          "entry_point": line["config"].get("entry_point"),
+                         "sfu": (line.get("roofline") or {}).get("secondary"),
                          "breakdown": {k: {"ms": v["ms"], "tflops": v["tflops"],
                                            "pct_of_peak": v.get("pct_of_peak")}
                                        for k, v in line.get("breakdown", {}).items()}}

@@ -52,3 +52,22 @@ def test_failed_side_run_is_reported_not_raised(monkeypatch):
     for cmd in calls:  # every side run is a bounded, single-purpose bench process
         assert "--no-also" in cmd and "--cpu-budget" in cmd
         assert cmd[cmd.index("--steps") + 1] == "100"
+
+
+def test_visible_scores_and_sfu_bound():
+    """The exponential count of the secondary bound: one per (row, visible key), causal rows
+    seeing keys j <= i; and the bound's arithmetic."""
+    import bench
+    import gen
+    w = gen.WORKLOADS["b2h8_n8192_d128_causal"]
+    assert bench.visible_scores(w) == 2 * 8 * 8192 * 8193 // 2
+    w = gen.WORKLOADS["b4h12_q1000_k4097_d64_cross"]
+    assert bench.visible_scores(w) == 4 * 12 * 1000 * 4097
+    w = gen.custom(1, 2, 10, 4, 64, gen.BF16, True)  # rows 3..9 see all 4 keys
+    assert bench.visible_scores(w) == 2 * (1 + 2 + 3 + 4 * 7)
+    w = gen.custom(1, 1, 3, 10, 64, gen.BF16, True)  # Nq < Nk: rows see 1, 2, 3 keys
+    assert bench.visible_scores(w) == 6
+    b = bench.sfu_bound(gen.WORKLOADS["b2h8_n8192_d128_causal"], ms=0.2, sms=152, sm_mhz=2000.0)
+    assert b["peak_ex2_per_s"] == 32 * 152 * 2000e6
+    assert abs(b["achieved_ex2_per_s"] - b["ex2_count"] / 0.2e-3) < 1
+    assert abs(b["pipe_frac_with_pack"] - 1.5 * b["frac"]) < 1e-3
