@@ -628,39 +628,31 @@ def _oracle_sample(budget_s: float, seed: int = 0):
     return total_flops / total_s / 1e12, total_s, threads, "; ".join(desc)
 
 
-def _oracle_single_core(budget_s: float = 2.0):
-    """The oracle on one thread: the two 128 x 128 d=64 workloads whole (full and causal),
-    and random rows of the d=64 cross-attention workload for about budget_s seconds."""
-    import numpy as np
-
+def _oracle_whole_configs(names=("tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross")):
+    """The oracle on whole configurations, end to end (the inputs already widened to
+    float64): the two 128 x 128 d=64 workloads and the d=64 cross-attention workload
+    (B=4, H=12, Nq=1000, Nk=4097; 50 GFLOP), each on all host threads and on one thread."""
     import gen
     import oracle
 
     out = {}
-    for name in ("tiny", "tiny_causal"):
+    for name in names:
         w = gen.WORKLOADS[name]
         q, k, v = (gen.to_f64_numpy(t) for t in gen.make_qkv(w))
-        reps, t0 = 0, time.perf_counter()
-        while True:
-            oracle.attention(q, k, v, w.scale, w.causal, nthreads=1)
-            reps += 1
-            dt = time.perf_counter() - t0
-            if dt >= 0.2:
-                break
-        out[name] = round(w.flops * reps / dt / 1e12, 6)
-    w = gen.WORKLOADS["b4h12_q1000_k4097_d64_cross"]
-    heads = tuple(gen.to_f64_numpy(t[:1, :1]) for t in gen.make_qkv(w))  # head (0, 0)
-    rng = np.random.default_rng(7)
-    n_rows, spent = 0, 0.0
-    while spent < budget_s:
-        rows = rng.integers(0, w.Nq, size=64)
-        t0 = time.perf_counter()
-        oracle.attention_rows(*heads, w.scale, w.causal, rows, nthreads=1)
-        spent += time.perf_counter() - t0
-        n_rows += rows.size
-    out[w.name] = round(4.0 * w.Nk * w.d * n_rows / spent / 1e12, 6)
-    out["sample"] = (f"one thread; tiny and tiny_causal whole; {n_rows} random rows of head (0,0) "
-                     f"of {w.name}, {spent:.1f} s")
+        res = {}
+        for label, nthreads in (("all_threads", oracle.hw_threads()), ("one_thread", 1)):
+            reps, t0 = 0, time.perf_counter()
+            while True:
+                oracle.attention(q, k, v, w.scale, w.causal, nthreads=nthreads)
+                reps += 1
+                dt = time.perf_counter() - t0
+                if dt >= 0.2:
+                    break
+            res[label] = {"ms": round(dt / reps * 1e3, 3), "tflops": round(w.flops * reps / dt / 1e12, 6),
+                          "threads": nthreads}
+        out[name] = res
+    out["note"] = ("whole configurations, float64, inputs already widened; the larger configurations are "
+                   "timed on row samples (cpu_baseline.value)")
     return out
 
 
@@ -669,9 +661,9 @@ def cpu_baseline(budget_s: float):
     line = {"value": round(tf, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{desc}; float64, {secs:.1f} s of host time; FLOPs 4*visible_keys*d per row"}
     try:
-        line["single_core"] = _oracle_single_core()
+        line["whole_configs"] = _oracle_whole_configs()
     except Exception as e:  # reported, never allowed to suppress the bench line
-        line["single_core"] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
+        line["whole_configs"] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
     return line
 
 

@@ -17,6 +17,9 @@ import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa.so")
+# The same library built with FA_DEBUG: every stream-K workspace access is range-checked on
+# the device and a violation is recorded as FA_ERR_BOUNDS (tests load it with load_library).
+DEBUG_LIB_PATH = os.path.join(PKG, "libfa_debug.so")
 
 FA_F16 = 0
 FA_BF16 = 1
@@ -26,7 +29,7 @@ STATUS = {
     -4: "FA_ERR_EMPTY_KEYS", -5: "FA_ERR_SCALE", -6: "FA_ERR_ALIGN", -7: "FA_ERR_DTYPE",
     -8: "FA_ERR_CUDA", -9: "FA_ERR_TENSOR_MAP", -10: "FA_ERR_DEVICE", -11: "FA_ERR_TIMEOUT",
     -12: "FA_ERR_WORKSPACE", -13: "FA_ERR_SCRATCH_LIMIT", -14: "FA_ERR_DROPOUT",
-    -15: "FA_ERR_RANGE",
+    -15: "FA_ERR_RANGE", -16: "FA_ERR_BOUNDS",
 }
 FA_WAIT_LIMIT_DEFAULT_US = 2_000_000
 FA_WAIT_LIMIT_MIN_US = 100
@@ -41,12 +44,13 @@ class FAError(RuntimeError):
         super().__init__(f"{what} failed: {STATUS.get(code, code)} ({strerror(code)})")
 
 
-def _load() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Open one build of the library (release or FA_DEBUG) with its C signatures declared."""
+    if not os.path.exists(path):
         raise ImportError(
-            f"libfa.so is not built ({LIB_PATH} missing); run __graft_entry__.build() first. "
-            "There is no fallback implementation.")
-    lib = ctypes.CDLL(LIB_PATH)
+            f"{os.path.basename(path)} is not built ({path} missing); run __graft_entry__.build() "
+            "first. There is no fallback implementation.")
+    lib = ctypes.CDLL(path)
     vp = ctypes.c_void_p
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp] + [ctypes.c_int] * 5 + [
@@ -99,10 +103,12 @@ def _load() -> ctypes.CDLL:
     lib.fa_set_wait_limit_us.argtypes = [ctypes.c_ulonglong]
     lib.fa_get_wait_limit_us.restype = ctypes.c_ulonglong
     lib.fa_get_wait_limit_us.argtypes = []
+    lib.fa_debug_cap_workspace.restype = ctypes.c_int
+    lib.fa_debug_cap_workspace.argtypes = [ctypes.c_longlong]
     return lib
 
 
-lib = _load()
+lib = load_library()
 
 
 def strerror(code: int) -> str:

@@ -30,21 +30,52 @@ def compile_cmd(out: str, extra=()) -> list[str]:
             *extra, SRC, "-o", out]
 
 
+# The same library with device-side range checks of every stream-K workspace access
+# (FA_DEBUG): an index outside the workspace's layout records FA_ERR_BOUNDS and the access
+# is skipped. Used by the tests; the release library compiles the checks out.
+DEBUG_LIB = os.path.join(PKG, "libfa_debug.so")
+DEBUG_FLAGS = ("-DFA_DEBUG",)
+
+
+def _stale(out: str) -> bool:
+    return not os.path.exists(out) or any(os.path.getmtime(out) < os.path.getmtime(d) for d in DEPS)
+
+
 def build(force: bool = False, verbose: bool = False, out: str = LIB, extra=()) -> str:
-    stale = force or not os.path.exists(out) or any(
-        os.path.getmtime(out) < os.path.getmtime(d) for d in DEPS)
-    if stale:
-        tmp = out + f".tmp{os.getpid()}"
-        cmd = compile_cmd(tmp, (*extra, "-Xptxas", "-v") if verbose else extra)
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            sys.stderr.write(r.stdout + r.stderr)
-            raise RuntimeError("nvcc failed building libfa.so")
+    return build_many([(out, extra)], force=force, verbose=verbose)[0]
+
+
+def build_many(targets, force: bool = False, verbose: bool = False) -> list[str]:
+    """Compile each (output, extra flags) target that is stale, all nvcc runs at once."""
+    procs = []
+    for out, extra in targets:
+        if force or _stale(out):
+            tmp = out + f".tmp{os.getpid()}"
+            cmd = compile_cmd(tmp, (*extra, "-Xptxas", "-v") if verbose else extra)
+            procs.append((out, tmp, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                                     text=True)))
+    failed = []
+    for out, tmp, pr in procs:
+        so, se = pr.communicate()
+        if pr.returncode != 0:
+            sys.stderr.write(so + se)
+            failed.append(os.path.basename(out))
+            continue
         if verbose:
-            sys.stderr.write(r.stderr)
+            sys.stderr.write(se)
         os.replace(tmp, out)
-    return out
+    if failed:
+        raise RuntimeError(f"nvcc failed building {', '.join(failed)}")
+    return [out for out, _ in targets]
+
+
+def build_all(force: bool = False) -> list[str]:
+    """The release library and its range-checked twin."""
+    return build_many([(LIB, ()), (DEBUG_LIB, DEBUG_FLAGS)], force=force)
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    if "--all" in sys.argv:
+        build_all(force="--force" in sys.argv)
+    else:
+        build(force="--force" in sys.argv, verbose="-v" in sys.argv)

@@ -27,6 +27,10 @@ using namespace fa;
 // Time limit of every device-side pipeline wait, read when a kernel is launched
 // (fa_set_wait_limit_us); 2 s unless the caller changes it.
 std::atomic<unsigned long long> g_wait_limit_ns{FA_WAIT_LIMIT_DEFAULT_US * 1000ull};
+// Debug builds only: the partial-state length the kernel is told is cut to this many floats
+// (negative: no cut), so that a test can make the range checks fire with every access still
+// inside the real workspace. Release builds leave it at -1.
+std::atomic<long long> g_debug_part_cap{-1};
 std::atomic<long long> g_launches{0};
 unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
@@ -245,6 +249,7 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
   p.streamk = 0;
   p.ws_part = nullptr;
   p.ws_cnt = nullptr;
+  p.ws_part_len = p.ws_cnt_len = 0;
   int grid = p.n_items < di->sms ? p.n_items : di->sms;
   // Full attention whose items do not fill whole waves of SMs: split the key range
   // (stream-K) when the caller provides the workspace.
@@ -254,6 +259,10 @@ int run(const void* Q, const void* K, const void* V, void* O, float* L, int B, i
     p.streamk = 1;
     p.ws_part = reinterpret_cast<float*>(workspace);
     p.ws_cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(workspace) + w.part_bytes);
+    p.ws_part_len = (long long)(w.part_bytes / sizeof(float));
+    p.ws_cnt_len = (long long)(w.cnt_bytes / sizeof(int));
+    const long long cap = g_debug_part_cap.load();
+    if (cap >= 0 && cap < p.ws_part_len) p.ws_part_len = cap;
     grid = w.G;
   }
 
@@ -382,6 +391,7 @@ int run_fp8(const void* Q, const void* K, const void* V, void* O, float* L, int 
   p.streamk = 0;
   p.ws_part = nullptr;
   p.ws_cnt = nullptr;
+  p.ws_part_len = p.ws_cnt_len = 0;
   p.o_scale = v_descale;
   p.drop_bias = 0;
   p.drop_offset = 0;
@@ -813,6 +823,16 @@ int fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O, c
                  workspace_bytes, stream, &da);
 }
 
+int fa_debug_cap_workspace(long long part_elems) {
+#ifdef FA_DEBUG
+  g_debug_part_cap.store(part_elems < 0 ? -1 : part_elems);
+  return 1;
+#else
+  (void)part_elems;
+  return 0;
+#endif
+}
+
 int fa_last_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
   int v = 0;
@@ -846,6 +866,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_DROPOUT:
       return "dropout probability must be finite, >= 0 and below 1 - 2^-9";
     case FA_ERR_RANGE: return "argument outside its documented range";
+    case FA_ERR_BOUNDS: return "device-side: a workspace index outside its layout (debug builds check)";
     default: return "unknown status code";
   }
 }

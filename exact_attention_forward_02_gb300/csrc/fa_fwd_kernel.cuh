@@ -138,7 +138,43 @@ struct Params {
   float* ws_part;  // partial states: [CTA][slot 2][Q tile 2][D + 2][128 rows] fp32 (O~, m, l),
                    // stored column by column so that a warp's accesses are coalesced
   int* ws_cnt;     // per (item, Q tile): K/V tiles accounted for; back to 0 after use
+  long long ws_part_len, ws_cnt_len;  // their lengths in elements (checked by debug builds)
 };
+
+// Debug builds (FA_DEBUG) check every stream-K workspace access against the workspace's
+// layout: an index outside it records FA_ERR_BOUNDS in the status word and the access is
+// skipped or redirected to the workspace's start (never a trap). Release builds compile the
+// checks out.
+__device__ __forceinline__ bool ws_in_range(long long first, long long count, long long len) {
+#ifdef FA_DEBUG
+  if (first < 0 || count < 0 || first + count > len) {
+    atomicCAS(&g_fa_status, 0, FA_ERR_BOUNDS);
+    return false;
+  }
+#else
+  (void)first;
+  (void)count;
+  (void)len;
+#endif
+  return true;
+}
+
+// Debug builds also check the coordinates of every TMA tile copy against the tensor's
+// extents (x the innermost, in elements): x on a 16-byte boundary and the tile's first
+// element inside the tensor. A load outside is recorded only (TMA fills what lies outside,
+// and the load's barrier still expects its bytes); a store outside is recorded and skipped.
+__device__ __forceinline__ bool tile_in_range(int x, int y, int z, int xdim, int ydim, int zdim,
+                                              int esz) {
+#ifdef FA_DEBUG
+  if (x < 0 || (x * esz) % 16 != 0 || x >= xdim || y < 0 || y >= ydim || z < 0 || z >= zdim) {
+    atomicCAS(&g_fa_status, 0, FA_ERR_BOUNDS);
+    return false;
+  }
+#else
+  (void)x, (void)y, (void)z, (void)xdim, (void)ydim, (void)zdim, (void)esz;
+#endif
+  return true;
+}
 
 // ----------------------------------------------------------------------------- waits
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -383,8 +419,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(full, LY::TILE_BYTES);
         const uint32_t dst = sKV + slot * LY::TILE_BYTES;
         if (FP8 && is_v) {  // V^T tile: D rows (head dims) x 128 keys starting at key row0
+          tile_in_range(row0, 0, bh, p.Nk, D, p.BH, 1);
           tma_load_3d_hint(dst, tm, full, row0, 0, bh, pol_kv);
         } else {
+          tile_in_range(0, row0, bh, D, p.Nk, p.BH, 128 / LY::CHUNK_ELEMS);
 #pragma unroll
           for (int c = 0; c < LY::CHUNKS; ++c)
             tma_load_3d_hint(dst + c * LY::CHUNK_BYTES, tm, full, c * LY::CHUNK_ELEMS, row0, bh,
@@ -405,6 +443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         q_ph ^= 1;
         const uint32_t qf = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(qf, (it.has1 ? 2 : 1) * LY::TILE_BYTES);
+        tile_in_range(0, it.q0 + (it.has1 ? BM : 0), it.bh, D, p.Nq, p.BH, 128 / LY::CHUNK_ELEMS);
 #pragma unroll
         for (int c = 0; c < LY::CHUNKS; ++c)
           tma_load_3d_hint(sQ + c * LY::CHUNK_BYTES, &tmQ, qf, c * LY::CHUNK_ELEMS, it.q0, it.bh,
@@ -599,7 +638,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = q0 + g * BM + r;
         const bool valid = row < p.Nq;
         auto piece = [&](int cc) -> const float* {
-          return p.ws_part + (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
+          const long long base = (((long long)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM;
+          return p.ws_part + (ws_in_range(base, PART_COLS * BM, p.ws_part_len) ? base : 0) + r;
         };
         uint8_t* orow = reinterpret_cast<uint8_t*>(p.O) +
                         ((size_t)bh * p.Nq + (size_t)(valid ? row : 0)) * D * 2;
@@ -674,9 +714,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const StageCmd c = bars->cmd[g];
       if (c.kind == STAGE_EXIT) break;
       if (lane == 0) {
-        if (c.kind == STAGE_O_BOX)
-          tma_store_3d(&tmO, stg, c.x, c.y, c.z);
-        else
+        if (c.kind == STAGE_O_BOX) {
+          if (tile_in_range(c.x, c.y, c.z, D, p.Nq, p.BH, 2)) tma_store_3d(&tmO, stg, c.x, c.y, c.z);
+        }
+        else if (ws_in_range(c.dst - p.ws_part, c.bytes / 4, p.ws_part_len))
           bulk_store_s2g(c.dst, stg, c.bytes);
         bulk_commit();
         bulk_wait_read0();
@@ -690,7 +731,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_global();
           __threadfence();
           int* cnt = p.ws_cnt + (size_t)c.item * 2 + g;
-          last = atomicAdd(cnt, c.n_kv) + c.n_kv == p.n_kv_all;
+          last = ws_in_range((long long)c.item * 2 + g, 1, p.ws_cnt_len) &&
+                 atomicAdd(cnt, c.n_kv) + c.n_kv == p.n_kv_all;
           if (last) {
             atomicExch(cnt, 0);  // every piece is in: ready for the next call
             __threadfence();
@@ -971,7 +1013,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // warp counts the piece (and merges if that completes the count).
           int* cnt = p.ws_cnt + (size_t)it.item * 2 + g;
           if (r == 0) {
-            bars->merge_now[g] = ld_acquire_gpu(cnt) + it.n_kv == p.n_kv_all;
+            bars->merge_now[g] = ws_in_range((long long)it.item * 2 + g, 1, p.ws_cnt_len) &&
+                                 ld_acquire_gpu(cnt) + it.n_kv == p.n_kv_all;
             mbar_arrive(smem_u32(&bars->decided[g]));
           }
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->decided[g]), dec_ph, abort_flag, lim));
@@ -1008,8 +1051,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // with this item; every later piece is its CTA's first (slot 0)
             const int slot0 = sk_bound(c0, W, G) < ub ? 1 : 0;
             auto piece = [&](int cc) -> const float* {
-              return p.ws_part +
-                     (((size_t)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM + r;
+              const long long base = (((long long)cc * 2 + (cc == c0 ? slot0 : 0)) * 2 + g) * PART_COLS * BM;
+              return p.ws_part + (ws_in_range(base, PART_COLS * BM, p.ws_part_len) ? base : 0) + r;
             };
             const int me = blockIdx.x;
             const float oscale = (DROP ? p.drop_rscale : 1.f) * (FP8 ? p.o_scale : 1.f);

@@ -44,7 +44,9 @@ enum {
   FA_ERR_WORKSPACE = -12,  /* fa_fwd_ws: workspace missing or too small                   */
   FA_ERR_SCRATCH_LIMIT = -13, /* fa_fwd_noalloc: needs more than FA_NOALLOC_SCRATCH_BYTES  */
   FA_ERR_DROPOUT = -14,    /* dropout probability negative, not finite or too close to 1  */
-  FA_ERR_RANGE = -15       /* an argument outside its documented range                    */
+  FA_ERR_RANGE = -15,      /* an argument outside its documented range                    */
+  FA_ERR_BOUNDS = -16      /* device-side, debug builds only (FA_DEBUG): a workspace index
+                              outside its layout; the access was skipped                  */
 };
 
 /* Limits of fa_set_wait_limit_us, in microseconds: the default (2 s), the smallest and the
@@ -294,6 +296,16 @@ int fa_selftest_wait_timeout(int limit_us, void* stream);
  * fa_get_wait_limit_us -- the current limit in microseconds. */
 int fa_set_wait_limit_us(unsigned long long limit_us);
 unsigned long long fa_get_wait_limit_us(void);
+
+/* fa_debug_cap_workspace -- test hook of the range-checked build (compiled with FA_DEBUG,
+ * libfa_debug.so), which checks every stream-K workspace access and every TMA tile
+ * coordinate on the device and records FA_ERR_BOUNDS for one outside its range (the access
+ * is skipped, or for a load only recorded). In that build, later fa_fwd_ws launches tell the
+ * kernel that the partial-state area holds at most `part_elems` floats, so that the checks
+ * fire while every access still lies inside the real workspace; a negative value removes
+ * the cut. Returns 1 in the range-checked build; the release build ignores the call and
+ * returns 0. No CUDA call is made. */
+int fa_debug_cap_workspace(long long part_elems);
 
 /* fa_num_kernel_launches -- number of kernels libfa has launched in this process
  * (all devices), for accounting launches in a timed region. */

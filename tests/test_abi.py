@@ -33,6 +33,20 @@ def test_library_exports_every_declared_symbol():
     assert not missing, f"declared in include/*.h but not exported: {missing}"
 
 
+def test_debug_build_exports_the_same_symbols_and_answers_its_hook():
+    """libfa_debug.so (FA_DEBUG: device-side range checks) is the same C ABI; only it takes
+    the workspace cut of fa_debug_cap_workspace, which makes no CUDA call."""
+    import exact_attention_forward_02_gb300 as fa
+    dbg = fa.load_library(fa.DEBUG_LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(dbg, n)]
+    assert not missing, f"declared in include/*.h but not exported by the debug build: {missing}"
+    assert dbg.fa_debug_cap_workspace(0) == 1
+    assert dbg.fa_debug_cap_workspace(-1) == 1
+    assert fa.lib.fa_debug_cap_workspace(0) == 0
+    assert fa.lib.fa_debug_cap_workspace(-1) == 0
+    assert "debug" in fa.strerror(fa.FA_ERR_BOUNDS)
+
+
 def test_status_strings():
     import exact_attention_forward_02_gb300 as fa
     for code, name in fa.STATUS.items():

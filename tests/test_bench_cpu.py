@@ -18,11 +18,16 @@ def test_reference_run_is_bounded_for_any_step_count():
     assert bench.reference_step_budget(2, 3) == 10.0
 
 
-def test_single_core_oracle_figures(oracle_mod):
-    out = bench._oracle_single_core(budget_s=0.05)
-    for name in ("tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross"):
-        assert out[name] > 0, out
-    assert "one thread" in out["sample"]
+def test_whole_config_oracle_figures(oracle_mod):
+    """Whole configurations timed end to end on all threads and on one (the small ones here;
+    the bench adds the d=64 cross-attention workload)."""
+    out = bench._oracle_whole_configs(names=("tiny", "tiny_causal"))
+    for name in ("tiny", "tiny_causal"):
+        for label in ("all_threads", "one_thread"):
+            r = out[name][label]
+            assert r["ms"] > 0 and r["tflops"] > 0, out
+        assert out[name]["one_thread"]["threads"] == 1
+    assert "whole configurations" in out["note"]
 
 
 def test_failed_side_run_is_reported_not_raised(monkeypatch):
