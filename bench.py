@@ -78,18 +78,23 @@ def visible_scores(w) -> int:
     return w.B * w.H * per_head
 
 
-def sfu_bound(w, ms: float, sms: int, sm_mhz: float) -> dict:
+def sfu_bound(w, ms: float, sms: int, sm_mhz: float, counters=None) -> dict:
     """The secondary bound of the forward pass: its exponentials. One ex2 per visible score
-    runs on the special-function pipe, whose measured rate is 32 lanes per clock per SM; the
-    16-bit pack of P (one cvt per two scores) issues to the same pipe, so the pipe carries
-    1.5 lane operations per score."""
+    runs on the special-function (XU) pipe, whose measured rate is 32 lanes per clock per SM.
+    Where the committed ncu record of this kernel holds its XU warp-instruction count
+    (sm__inst_executed_pipe_xu.sum), that count is given beside the ex2 warp instructions
+    the scores need (ex2_count / 32): the ex2s are nearly all of the pipe's work."""
     n = visible_scores(w)
     peak = EX2_PER_CLK_PER_SM * sms * sm_mhz * 1e6
     achieved = n / (ms * 1e-3)
-    return {"bound": "sfu", "ex2_count": n, "achieved_ex2_per_s": achieved, "peak_ex2_per_s": peak,
-            "frac": round(achieved / peak, 4), "pipe_frac_with_pack": round(1.5 * achieved / peak, 4),
-            "peak_source": f"{EX2_PER_CLK_PER_SM} ex2/clk/SM x {sms} SMs x {sm_mhz:g} MHz (median SM clock "
-                           "sampled in the timed region)"}
+    out = {"bound": "sfu", "ex2_count": n, "achieved_ex2_per_s": achieved, "peak_ex2_per_s": peak,
+           "frac": round(achieved / peak, 4),
+           "peak_source": f"{EX2_PER_CLK_PER_SM} ex2/clk/SM x {sms} SMs x {sm_mhz:g} MHz (median SM clock "
+                          "sampled in the timed region)"}
+    if counters and counters.get("xu_inst"):
+        out["xu_inst_counted"] = counters["xu_inst"]
+        out["xu_inst_per_ex2_warp_inst"] = round(counters["xu_inst"] / (n / 32), 4)
+    return out
 
 
 def peaks():
@@ -110,16 +115,17 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, only
-    while the kernel source is the one those counters were taken on."""
+def recorded_counters(workload, entry: str):
+    """The committed ncu counters of the kernel that runs `workload` through `entry`
+    ("fa_fwd" or "fa_fwd_ws"), only while the kernel source is the one they were taken on."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         if rec.get("source_sha256") != kernel_source_hash():
             return None
-        return rec["kernels"][workload]["dram_bytes_per_launch"]
+        k = rec["kernels"][workload]
+        return k if k.get("entry") == entry else None
     except Exception:
         return None
 
@@ -399,6 +405,8 @@ def run_ours(args):
                           "fa_fwd" if devbuf[w.name][5] is None else
                           "fa_fwd_ws (stream-K split of the key range, caller workspace)")
                  for w in wl}
+        dom_entry = entry[dominant].split(" ")[0]
+        dom_counters = recorded_counters(dominant, dom_entry) if dom_entry in ("fa_fwd", "fa_fwd_ws") else None
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": n, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
@@ -419,9 +427,9 @@ def run_ours(args):
                          "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} dense (burst: kernel timed alone)",
-                         "traffic": recorded_traffic(dominant) if args.dropout == 0 else None,
+                         "traffic": (dom_counters or {}).get("dram_bytes_per_launch"),
                          "algorithmic_bytes": wd.io_bytes,
-                         "secondary": sfu_bound(wd, dom_ms, sms, sm_mhz)},
+                         "secondary": sfu_bound(wd, dom_ms, sms, sm_mhz, dom_counters)},
             "clocks": clk,
             "e2e": {"value": round(whole_job_tflops(flops_step, ws, e2e_ms_max), 2), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ne2e,

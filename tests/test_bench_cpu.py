@@ -75,4 +75,22 @@ def test_visible_scores_and_sfu_bound():
     b = bench.sfu_bound(gen.WORKLOADS["b2h8_n8192_d128_causal"], ms=0.2, sms=152, sm_mhz=2000.0)
     assert b["peak_ex2_per_s"] == 32 * 152 * 2000e6
     assert abs(b["achieved_ex2_per_s"] - b["ex2_count"] / 0.2e-3) < 1
-    assert abs(b["pipe_frac_with_pack"] - 1.5 * b["frac"]) < 1e-3
+    assert "xu_inst_counted" not in b
+    b = bench.sfu_bound(gen.WORKLOADS["b2h8_n8192_d128_causal"], ms=0.2, sms=152, sm_mhz=2000.0,
+                        counters={"xu_inst": b["ex2_count"] // 32 * 103 // 100})
+    assert b["xu_inst_per_ex2_warp_inst"] == 1.03
+
+
+def test_recorded_counters_match_source_and_entry():
+    """The committed ncu record is used only for the kernel source it was taken on and for
+    the entry point it was taken through; its XU count covers the ex2s the scores need."""
+    import json
+    import bench
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    for name, k in rec["kernels"].items():
+        assert k["dram_bytes_per_launch"] == k["read"] + k["write"]
+        assert 1.0 <= k["xu_inst"] / k["ex2_warp_inst"] < 1.1, name
+        if rec["source_sha256"] == bench.kernel_source_hash():
+            assert bench.recorded_counters(name, k["entry"]) == k
+            other = "fa_fwd" if k["entry"] == "fa_fwd_ws" else "fa_fwd_ws"
+            assert bench.recorded_counters(name, other) is None
