@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_workspace_bytes.argtypes = [ctypes.c_int] * 6
     lib.fa_last_status.restype = ctypes.c_int
     lib.fa_last_status.argtypes = []
+    lib.fa_stream_status.restype = ctypes.c_int
+    lib.fa_stream_status.argtypes = [vp]
     lib.fa_clear_status.restype = ctypes.c_int
     lib.fa_clear_status.argtypes = []
     lib.fa_strerror.restype = ctypes.c_char_p
@@ -202,6 +204,11 @@ def fa_bwd_workspace_bytes(B, H, Nq, Nk, d) -> int:
 
 def fa_last_status() -> int:
     return int(lib.fa_last_status())
+
+
+def fa_stream_status(stream=None) -> int:
+    """The device-side status once `stream`'s queued work has finished (that stream only)."""
+    return int(lib.fa_stream_status(stream))
 
 
 def fa_clear_status() -> int:

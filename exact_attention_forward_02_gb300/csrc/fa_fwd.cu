@@ -840,6 +840,16 @@ int fa_last_status(void) {
   return v;
 }
 
+int fa_stream_status(void* stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  // queued behind the stream's work; the wait covers this stream only
+  if (cudaMemcpyFromSymbolAsync(&v, g_fa_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return v;
+}
+
 int fa_clear_status(void) {
   const int z = 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;

@@ -267,6 +267,13 @@ int fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O, c
  * synchronisation itself fails. */
 int fa_last_status(void);
 
+/* fa_stream_status -- the same status word, read once the work already queued on `stream`
+ * (NULL: the legacy default stream) has finished; other streams are not waited for. The
+ * word is shared by every launch of libfa on the device, so it may also hold an error that
+ * a kernel on another stream recorded. Returns the status, or FA_ERR_CUDA if the read or the
+ * stream synchronisation fails. */
+int fa_stream_status(void* stream);
+
 /* fa_clear_status -- reset the device-side status word of the current device to FA_OK.
  * Returns FA_OK or FA_ERR_CUDA. */
 int fa_clear_status(void);

@@ -183,6 +183,29 @@ def test_bounded_wait_times_out_cleanly_and_context_survives():
     assert r["raw_ok"], r
 
 
+def test_stream_status_waits_for_its_stream_only():
+    """fa_stream_status reads the status word behind one stream's work: FA_OK after a
+    forward pass on a side stream, FA_ERR_TIMEOUT after the self test queued there."""
+    import exact_attention_forward_02_gb300 as fa
+    assert fa.fa_clear_status() == 0
+    s = torch.cuda.Stream()
+    sp = ctypes.c_void_p(s.cuda_stream)
+    w = gen.WORKLOADS["tiny"]
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in gen.make_qkv(w))
+    torch.cuda.current_stream().synchronize()
+    O = torch.empty((w.B, w.H, w.Nq, w.d), dtype=q.dtype, device=dev)
+    L = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(s):
+        assert fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(),
+                         w.B, w.H, w.Nq, w.Nk, w.d, w.scale, w.causal, fa.FA_F16, sp) == 0
+    assert fa.fa_stream_status(sp) == fa.FA_OK
+    assert fa.fa_selftest_wait_timeout(1000, sp) == 0
+    assert fa.fa_stream_status(sp) == fa.FA_ERR_TIMEOUT
+    assert fa.fa_clear_status() == 0
+    assert fa.fa_stream_status(sp) == fa.FA_OK
+
+
 def test_wait_limit_applies_to_later_launches():
     """A raised library-wide wait limit is taken by the next launches (the forward pass
     completes with status 0 under it); the self test still times out at its own limit."""
