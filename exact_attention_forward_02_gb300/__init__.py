@@ -17,8 +17,10 @@ import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa.so")
-# The same library built with FA_DEBUG: every stream-K workspace access is range-checked on
-# the device and a violation is recorded as FA_ERR_BOUNDS (tests load it with load_library).
+# The same library built with FA_DEBUG: every stream-K workspace access and TMA tile
+# coordinate of the forward kernel is range-checked on the device, and a violation is
+# recorded as FA_ERR_BOUNDS. Tests load it with load_library; FA_LIBRARY=debug in the
+# environment makes it the library this module binds.
 DEBUG_LIB_PATH = os.path.join(PKG, "libfa_debug.so")
 
 FA_F16 = 0
@@ -110,7 +112,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     return lib
 
 
-lib = load_library()
+_choice = os.environ.get("FA_LIBRARY", "release")
+if _choice not in ("release", "debug"):
+    raise ImportError(f"FA_LIBRARY must be 'release' or 'debug', not {_choice!r}")
+lib = load_library(DEBUG_LIB_PATH if _choice == "debug" else LIB_PATH)
 
 
 def strerror(code: int) -> str:

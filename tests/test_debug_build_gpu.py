@@ -24,10 +24,11 @@ def libs():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import exact_attention_forward_02_gb300 as fa
+    rel = fa.load_library(fa.LIB_PATH)
     dbg = fa.load_library(fa.DEBUG_LIB_PATH)
-    assert dbg.fa_clear_status() == 0 and fa.fa_clear_status() == 0
+    assert dbg.fa_clear_status() == 0 and rel.fa_clear_status() == 0
     assert dbg.fa_debug_cap_workspace(-1) == 1
-    yield fa, fa.lib, dbg
+    yield fa, rel, dbg
     dbg.fa_debug_cap_workspace(-1)
 
 
