@@ -19,15 +19,19 @@ def test_reference_run_is_bounded_for_any_step_count():
 
 
 def test_whole_config_oracle_figures(oracle_mod):
-    """Whole configurations timed end to end on all threads and on one (the small ones here;
-    the bench adds the d=64 cross-attention workload)."""
-    out = bench._oracle_whole_configs(names=("tiny", "tiny_causal"))
-    for name in ("tiny", "tiny_causal"):
-        for label in ("all_threads", "one_thread"):
-            r = out[name][label]
-            assert r["ms"] > 0 and r["tflops"] > 0, out
-        assert out[name]["one_thread"]["threads"] == 1
+    """Whole configurations timed end to end on all threads and, where asked, on one (the
+    small ones here; the bench adds the d=64 cross-attention and the two benchmark
+    workloads)."""
+    out = bench._oracle_whole_configs(configs=(("tiny", True), ("tiny_causal", False)))
+    for label in ("all_threads", "one_thread"):
+        r = out["tiny"][label]
+        assert r["ms"] > 0 and r["tflops"] > 0, out
+    assert out["tiny"]["one_thread"]["threads"] == 1
+    assert set(out["tiny_causal"]) == {"all_threads"}
     assert "whole configurations" in out["note"]
+    names = [n for n, _ in bench.WHOLE_CONFIGS]
+    assert {"tiny", "tiny_causal", "b4h12_q1000_k4097_d64_cross", "b2h8_n4096_d128_full",
+            "b2h8_n8192_d128_causal"} == set(names)
 
 
 def test_failed_side_run_is_reported_not_raised(monkeypatch):
