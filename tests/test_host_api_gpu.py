@@ -71,3 +71,16 @@ def test_host_api_full_size_workload():
     O0, L0 = run_cuda(w, q, k, v)
     O1, L1 = run_host(w, q, k, v, True)
     assert torch.equal(O0, O1) and torch.equal(L0, L1)
+
+
+def test_host_api_full_size_full_attention():
+    """The full N=4096 workload through fa_fwd_host (chunks of 8, 6 and 2 heads): every
+    element of O and L against the oracle, and bit for bit against fa_fwd."""
+    from tests.fa_testlib import compare, oracle_whole
+    w = gen.WORKLOADS["b2h8_n4096_d128_full"]
+    (q, k, v), (Oref, Lref) = oracle_whole(w.name)
+    O1, L1 = run_host(w, q, k, v, True)
+    r = compare(w, O1, L1, Oref, Lref)
+    assert r["raw_ok"], r
+    O0, L0 = run_cuda(w, q, k, v)
+    assert torch.equal(O0, O1) and torch.equal(L0, L1)
