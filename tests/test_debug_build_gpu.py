@@ -70,6 +70,7 @@ CASES = [
     (1, 1, 3, 300, 128, gen.F16, False, "fa_fwd_ws"),
     (1, 2, 1000, 1000, 128, gen.BF16, True, "fa_fwd"),     # causal, ragged Q tail
     (2, 3, 300, 4097, 64, gen.F16, False, "fa_fwd"),
+    (8, 64, 256, 256, 64, gen.F16, False, "fa_fwd_ws"),    # ranges over several short items
 ]
 
 

@@ -63,6 +63,8 @@ SMALL = [
     (1, 2, 512, 512, 64, gen.F16, False, 3.0),
     (4, 16, 1024, 1024, 64, gen.F16, True, 1.0),     # 256 work items: several per CTA
     (2, 40, 512, 640, 128, gen.BF16, False, 1.0),    # 160 work items: > one per SM
+    (8, 64, 256, 256, 64, gen.F16, False, 1.0),      # 512 heads of one work item each
+    (16, 32, 200, 200, 128, gen.BF16, True, 1.0),    # 512 heads, one ragged causal item each
 ]
 
 

@@ -53,6 +53,7 @@ CASES = [
     (1, 1, 3, 300, 128, gen.F16),
     (2, 40, 512, 640, 128, gen.BF16),      # 160 items on 152 SMs
     (4, 12, 1000, 4097, 64, gen.F16),      # the cross-attention workload's shape
+    (8, 64, 256, 256, 64, gen.F16),        # 512 items of 2 K/V tiles: ranges span several
 ]
 
 
