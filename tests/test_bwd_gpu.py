@@ -56,6 +56,20 @@ def test_bwd_matches_oracle(case):
         assert e["max_abs_err"] <= TOL_REL[dt] * max(e["max_abs_ref"], 0.05), (name, e)
 
 
+@pytest.mark.parametrize("name", ["b2h8_n4096_d128_full", "b2h8_n8192_d128_causal"])
+def test_bwd_full_size_workloads(name):
+    """The backward of the two benchmark workloads at full size, as `bench.py --bwd` runs
+    it: every element of dQ, dK and dV against the float64 oracle."""
+    w = gen.WORKLOADS[name]
+    q, k, v, do = make_inputs(w)
+    O, L, dQ, dK, dV = run_fwd_bwd(w, q, k, v, do)
+    errs = grad_errors(w, q, k, v, do, dQ, dK, dV)
+    print(w.name, errs)
+    for gname, e in errs.items():
+        assert e["finite"], gname
+        assert e["max_abs_err"] <= TOL_REL[w.dtype] * max(e["max_abs_ref"], 0.05), (gname, e)
+
+
 def test_bwd_deterministic():
     w = gen.custom(2, 3, 500, 500, 128, gen.BF16, True, 1.0, seed=99)
     q, k, v, do = make_inputs(w)
