@@ -21,7 +21,7 @@ import pytest
 import torch
 
 import gen
-from tests.fa_testlib import TOL_L, half_ulp, sample_rows
+from tests.fa_testlib import TOL_L, half_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -150,13 +150,14 @@ def test_fp8_matches_oracle(oracle_mod, case):
 
 
 @pytest.mark.parametrize("name", sorted(gen.FP8_WORKLOADS))
-def test_fp8_full_size_sampled_rows(oracle_mod, name):
+def test_fp8_full_size_whole_output(oracle_mod, name):
+    """The E4M3 versions of the two benchmark workloads at full size: every element of O and
+    L against the oracle on the decoded inputs, with the bound of the E4M3 rounding of P."""
     w = gen.FP8_WORKLOADS[name]
     q, k, v = gen.make_qkv(w)
     O, L = run_fp8(q, k, v, w.scale, w.causal)
-    rows = sample_rows(w, n_heads=3, n_rand=6)
     print(name, "max err, rms err, mean bound",
-          check(q, k, v, O, L, w.scale, w.causal, 1.0, 1.0, 1.0, gen.BF16, rows))
+          check(q, k, v, O, L, w.scale, w.causal, 1.0, 1.0, 1.0, gen.BF16))
 
 
 def test_fp8_errors_and_determinism():
