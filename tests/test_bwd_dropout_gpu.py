@@ -89,6 +89,26 @@ def test_dropout_bwd_matches_oracle(oracle_mod, case):
         assert err <= bound, (name, err, bound)
 
 
+@pytest.mark.parametrize("name", ["b2h8_n4096_d128_full", "b2h8_n8192_d128_causal"])
+def test_dropout_bwd_full_size_workloads(oracle_mod, name):
+    """The dropout backward of the two benchmark workloads at full size (p = 0.1, as
+    `bench.py --bwd --dropout 0.1` runs it): every element of dQ, dK and dV."""
+    w = gen.WORKLOADS[name]
+    q, k, v, do = make_inputs(w)
+    p, seed, off = 0.1, 1234, 1
+    O, L, dQ, dK, dV = run_drop_fwd_bwd(w, q, k, v, do, p, seed, off)
+    rq, rk, rv = oracle_mod.attention_bwd_dropout(gen.to_f64_numpy(q), gen.to_f64_numpy(k),
+                                                  gen.to_f64_numpy(v), gen.to_f64_numpy(do), w.scale,
+                                                  w.causal, _f32(p), seed, off)
+    for gname, got, ref in (("dQ", dQ, rq), ("dK", dK, rk), ("dV", dV, rv)):
+        g = got.double().numpy()
+        assert np.isfinite(g).all(), gname
+        err = float(np.abs(g - ref).max())
+        bound = TOL_REL[w.dtype] * max(float(np.abs(ref).max()), 0.05)
+        print(name, gname, "max err", err, "bound", bound)
+        assert err <= bound, (gname, err, bound)
+
+
 def test_zero_probability_is_fa_bwd_and_bad_probability():
     import exact_attention_forward_02_gb300 as fa
     w = gen.custom(1, 2, 300, 300, 128, gen.BF16, True, 1.0, seed=12)
